@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for the attention forward: BF16 Q, K, V ~ N(0, 1).
+
+This module is the only code shared by the CUDA path's callers (tests, bench)
+and the FP64 oracle. It holds no attention arithmetic: it only draws numbers.
+
+Recipe (fixed, so a seed names one input on every machine that runs it):
+
+* counter-based generator: SplitMix64 (Steele, Lea and Flood, "Fast splittable
+  pseudorandom number generators", OOPSLA 2014; finaliser constants as
+  published by Vigna). Element ``i`` of stream ``s`` under seed ``seed`` is the
+  finaliser applied to ``key(seed, s) + (i + 1) * GAMMA``.
+* normal deviates: Box-Muller on pairs of 53-bit uniforms, in float64.
+* storage: float64 -> float32 (round to nearest even) -> bfloat16 (round to
+  nearest even), kept as raw ``uint16`` bit patterns.
+* "1% of K rows scaled by 8": for each (batch, kv-head), ``round(0.01 * N_k)``
+  rows are picked without replacement (the rows with the smallest draws of a
+  separate stream) and multiplied by 8, which is exact in bfloat16.
+
+Layouts: Q is ``[B][H_q][N_q][d]``, K and V are ``[B][H_kv][N_k][d]``, all
+contiguous row-major.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+STREAM_Q, STREAM_K, STREAM_V, STREAM_ROWS = 1, 2, 3, 4
+
+_CHUNK = 1 << 22  # elements generated per numpy pass (bounds temporaries)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 output finaliser on a uint64 array (wrapping arithmetic)."""
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _stream_key(seed: int, stream: int) -> np.uint64:
+    x = np.array([(seed * 0x100000001B3 + stream * 0x632BE59BD9B4E019) & (2**64 - 1)],
+                 dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(x + GAMMA)[0]
+
+
+def uniform_u64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Raw 64-bit draws ``start .. start+count-1`` of one stream."""
+    key = _stream_key(seed, stream)
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(key + idx * GAMMA)
+
+
+def normal_f64(seed: int, stream: int, count: int) -> np.ndarray:
+    """``count`` standard normal deviates (Box-Muller), float64."""
+    return _normal_slice(seed, stream, 0, count)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float64 -> float32 (RNE) -> bfloat16 (RNE); returns uint16 bit patterns."""
+    f = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = (f + np.uint32(0x7FFF) + ((f >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float32."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
+    count = int(np.prod(shape))
+    out = np.empty(count, dtype=np.uint16)
+    for lo in range(0, count, 2 * _CHUNK):
+        hi = min(count, lo + 2 * _CHUNK)
+        # draw the whole stream prefix-consistently: element i always uses pair i//2
+        z = _normal_slice(seed, stream, lo, hi)
+        out[lo:hi] = f64_to_bf16_bits(z)
+    return out.reshape(shape)
+
+
+def _normal_slice(seed: int, stream: int, lo: int, hi: int) -> np.ndarray:
+    """Normal deviates for elements [lo, hi) of a stream (lo even)."""
+    assert lo % 2 == 0
+    p0, p1 = lo // 2, (hi + 1) // 2
+    r = uniform_u64(seed, stream, 2 * p0, 2 * (p1 - p0))
+    a = (r[0::2] >> np.uint64(11)).astype(np.float64)
+    b = (r[1::2] >> np.uint64(11)).astype(np.float64)
+    u1 = (a + 1.0) * (1.0 / 9007199254740992.0)
+    u2 = b * (1.0 / 9007199254740992.0)
+    rad = np.sqrt(-2.0 * np.log(u1))
+    ang = 2.0 * math.pi * u2
+    z = np.empty(2 * (p1 - p0), dtype=np.float64)
+    z[0::2] = rad * np.cos(ang)
+    z[1::2] = rad * np.sin(ang)
+    return z[: hi - lo]
+
+
+def scaled_rows(seed: int, n_bh: int, n_k: int, frac: float) -> np.ndarray:
+    """Row indices (per flattened (batch, kv-head)) chosen for the x8 scaling.
+
+    Returns an int64 array of shape ``[n_bh, round(frac * n_k)]``.
+    """
+    n_pick = int(round(frac * n_k))
+    picks = np.empty((n_bh, n_pick), dtype=np.int64)
+    for bh in range(n_bh):
+        r = uniform_u64(seed, STREAM_ROWS, bh * n_k, n_k)
+        picks[bh] = np.sort(np.argsort(r, kind="stable")[:n_pick])
+    return picks
+
+
+@dataclasses.dataclass
+class AttentionInputs:
+    """One seeded problem. Arrays hold bfloat16 bit patterns (uint16)."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    B: int
+    H_q: int
+    H_kv: int
+    N_q: int
+    N_k: int
+    d: int
+    causal: bool
+    scale: float
+
+    @property
+    def shape_args(self):
+        return (self.B, self.H_q, self.H_kv, self.N_q, self.N_k, self.d)
+
+
+def make_inputs(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int, *,
+                causal: bool = False, scale: float | None = None, seed: int = 0,
+                k_row_frac: float = 0.0, k_row_factor: float = 8.0) -> AttentionInputs:
+    """Draw Q, K, V for one configuration (all BF16 ~ N(0, 1))."""
+    q = normal_bf16(seed, STREAM_Q, (B, H_q, N_q, d))
+    k = normal_bf16(seed, STREAM_K, (B, H_kv, N_k, d))
+    v = normal_bf16(seed, STREAM_V, (B, H_kv, N_k, d))
+    if k_row_frac > 0.0:
+        rows = scaled_rows(seed, B * H_kv, N_k, k_row_frac)
+        kf = k.reshape(B * H_kv, N_k, d)
+        for bh in range(B * H_kv):
+            sel = kf[bh, rows[bh]]
+            kf[bh, rows[bh]] = f64_to_bf16_bits(bf16_bits_to_f32(sel).astype(np.float64) * k_row_factor)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return AttentionInputs(q, k, v, B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale))
+
+
+# The five workloads the method is measured on (batch, heads, lengths, head dim,
+# mask, K-row stress), with their names. Seed 0 throughout.
+WORKLOADS = {
+    "tiny_n256_d64": dict(B=1, H_q=1, H_kv=1, N_q=256, N_k=256, d=64, causal=False),
+    "one_head_n8192_d128": dict(B=1, H_q=1, H_kv=1, N_q=8192, N_k=8192, d=128, causal=False),
+    "h32_n4096_d128": dict(B=1, H_q=32, H_kv=32, N_q=4096, N_k=4096, d=128, causal=False),
+    "h32_n4096_d128_causal": dict(B=1, H_q=32, H_kv=32, N_q=4096, N_k=4096, d=128, causal=True),
+    "h32_n16384_d128_causal_krows": dict(B=1, H_q=32, H_kv=32, N_q=16384, N_k=16384, d=128,
+                                         causal=True, k_row_frac=0.01),
+    "h32_n32768_d128_causal_krows": dict(B=1, H_q=32, H_kv=32, N_q=32768, N_k=32768, d=128,
+                                         causal=True, k_row_frac=0.01),
+    "decode_b16_h32_kv8_n8192_d128": dict(B=16, H_q=32, H_kv=8, N_q=1, N_k=8192, d=128,
+                                          causal=False),
+}
+
+
+def make_workload(name: str, seed: int = 0) -> AttentionInputs:
+    return make_inputs(seed=seed, **WORKLOADS[name])

@@ -1,0 +1,33 @@
+"""FP64 CPU oracle for the exact attention forward — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it, and it
+shares no code, header, table or constant with the CUDA library: the only
+thing both sides consume is the seeded input buffer drawn by
+``exact_tiled_attention_forward_gb300.inputs`` (which holds no attention
+arithmetic).
+
+Contents
+--------
+``attention``  the definition ``O = softmax(scale * Q K^T) V`` written out in
+               FP64 with the score and probability matrices materialised
+               (row block by row block), plus the per-row log-sum-exp; a
+               tiled online-softmax restatement used as a self-check; a
+               pure-Python brute force for tiny shapes; the split merge.
+``traffic``    the pages' analytic HBM byte and FLOP counts.
+
+Every function names the page and section it follows. Each is pinned in
+``tests/test_oracle_*.py`` against values the pages print, closed forms and
+invariants (see the test files for the pin of each function).
+"""
+from .attention import (  # noqa: F401
+    bf16_to_f64,
+    attention_reference,
+    attention_rows,
+    attention_tiled_online,
+    online_softmax_blocks,
+    brute_force_attention,
+    merge_partials,
+    visible_key_count,
+)
+from . import traffic  # noqa: F401
