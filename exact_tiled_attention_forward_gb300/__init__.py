@@ -1,5 +1,158 @@
 """Exact tiled attention forward (FlashAttention forward) for GB300 / sm_103a.
 
-The compute path is the C-ABI library ``libfa`` (hand-written CUDA kernels);
-this package holds its Python binding and the seeded input generator.
+The compute path is the C-ABI library ``libfa`` (``include/fa.h``): hand-written
+CUDA kernels built for sm_103a by ``build.py``. This module is a thin binding
+with the same entry-point names; it only marshals arguments (device pointers,
+sizes, the current CUDA stream). There is no fallback: if ``libfa.so`` is
+missing or fails to load, every call raises.
+
+    import exact_tiled_attention_forward_gb300 as fa
+    o, lse = fa.fa_forward(q, k, v, causal=False)          # torch CUDA tensors
+
+Tensors: q ``[B, H_q, N_q, d]``, k/v ``[B, H_kv, N_k, d]`` BF16 contiguous;
+returns o ``[B, H_q, N_q, d]`` BF16 and lse ``[B, H_q, N_q]`` FP32.
 """
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libfa.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_CUDA = -3
+FA_ERR_NO_MEMORY = -4
+FA_ERR_TIMEOUT = -5
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = lib().fa_status_string(status).decode()
+        if status == FA_ERR_CUDA:
+            msg += f" (cudaError {lib().fa_get_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+_SIGNATURES = {
+    "fa_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
+                         [_c_float, _vp, _c_size, _vp]),
+    "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
+    "fa_status_string": (ctypes.c_char_p, [_c_int]),
+    "fa_get_last_cuda_error": (_c_int, []),
+    "fa_device_status": (_c_int, [_c_int]),
+    "fa_version": (_c_int, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libfa.so not found at {LIB_PATH}: build it first "
+                              "(python -m exact_tiled_attention_forward_gb300.build)")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/fa.h`` declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims(q, k):
+    B, H_q, N_q, d = q.shape
+    Bk, H_kv, N_k, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k/v disagree on batch or head dim")
+    return B, H_q, H_kv, N_q, N_k, d
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
+
+
+def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+               return_lse: bool = True, stream=None):
+    """Fused forward on the current CUDA stream. Returns ``(o, lse)``."""
+    import torch
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    st = lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q, N_k,
+                          d, int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "fa_forward")
+    return out, lse
+
+
+def fa_naive_workspace_bytes(B: int, H_q: int, N_q: int, N_k: int) -> int:
+    return int(lib().fa_naive_workspace_bytes(B, H_q, N_q, N_k))
+
+
+def fa_naive_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                     lse=None, workspace=None, return_lse: bool = True, stream=None):
+    """Unfused three-kernel baseline. Returns ``(o, lse)``."""
+    import torch
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    nbytes = fa_naive_workspace_bytes(B, H_q, N_q, N_k)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().fa_naive_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q,
+                                N_k, d, int(bool(causal)), float(scale), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(st, "fa_naive_forward")
+    return out, lse
+
+
+def fa_device_status(reset: bool = True) -> int:
+    """Synchronise and return the device status word (FA_OK or FA_ERR_TIMEOUT)."""
+    return int(lib().fa_device_status(int(bool(reset))))
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(status).decode()
+
+
+def fa_version() -> tuple[int, int]:
+    v = int(lib().fa_version())
+    return v >> 16, v & 0xFFFF

@@ -1,0 +1,307 @@
+// C ABI of libfa: argument validation, tensor-map construction, work split
+// and launches. Declared in include/fa.h.
+#include "fa_internal.h"
+#include "fa.h"
+
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+namespace fa {
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+__device__ int g_device_status;  // one per device (module-scope device variable)
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return FA_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct Shape {
+  int B, H_q, H_kv, N_q, N_k, d;
+};
+
+// Shared validation of the fa_forward / fa_naive_forward arguments.
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const Shape& s, float scale) {
+  if (s.B < 0 || s.N_q < 0 || s.N_k < 0 || s.H_q < 1 || s.H_kv < 1 || s.d < 1)
+    return FA_ERR_INVALID_ARG;
+  if (s.H_q % s.H_kv != 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  // indices inside the kernels are 32-bit per (batch*head) row
+  const long long rows_q = (long long)s.B * s.H_q * s.N_q;
+  const long long rows_k = (long long)s.B * s.H_kv * s.N_k;
+  if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
+  if (rows_q == 0) return FA_OK;  // nothing to write
+  if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if (rows_k > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+  const size_t qb = (size_t)rows_q * s.d * 2, kb = (size_t)rows_k * s.d * 2;
+  const size_t lb = lse ? (size_t)rows_q * 4 : 0;
+  // outputs may not overlap any input or each other
+  if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb))
+    return FA_ERR_INVALID_ARG;
+  if (lse && (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+              overlaps(lse, lb, o, qb)))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// O = 0, LSE = -inf for every row (no key at all: N_k == 0)
+__global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, long long rows, int d) {
+  const long long n = rows * d;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    o[i] = __float2bfloat16_rn(0.f);
+    if (lse && i < rows) lse[i] = -INFINITY;
+  }
+}
+
+int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st) {
+  fill_empty_kernel<<<256, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(o), lse, rows, d);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+// Splits per query block when there are too few blocks to fill the GPU.
+// Cost model: waves * (2 + tiles per split), in units of one K/V tile step.
+int choose_splits(long long blocks, int kv_tiles, int sms) {
+  if (kv_tiles <= 1 || blocks >= 2ll * sms) return 1;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= 16 && s <= kv_tiles; ++s) {
+    const long long units = blocks * s;
+    const long long waves = (units + sms - 1) / sms;
+    const double cost = (double)waves * (2.0 + (double)kv_tiles / s);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {row_stride_elems * 2, row_stride_elems * 2 * rows};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* device_status_ptr() {
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return (0 << 16) | 1; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_NO_MEMORY: return "out of memory / workspace too small";
+    case FA_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_get_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fa_device_status(int reset) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int* p = device_status_ptr();
+  if (!p) return cuda_fail(cudaGetLastError());
+  int h = 0;
+  e = cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (reset && h != 0) {
+    int zero = 0;
+    e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return h == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k) {
+  if (B < 0 || H_q < 1 || N_q < 0 || N_k < 0) return 0;
+  const size_t ld = ((size_t)N_k + 7) / 8 * 8;
+  return (size_t)B * H_q * N_q * ld * 2;
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+               int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream) {
+  const Shape s{B, H_q, H_kv, N_q, N_k, d};
+  int st = validate(q, k, v, o, lse, s, scale);
+  if (st != FA_OK) return st;
+  if ((long long)B * H_q * N_q == 0) return FA_OK;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  if (N_k == 0 || B * H_kv == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
+
+  int* status = device_status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+
+  FwdParams p{};
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+  p.causal = causal ? 1 : 0;
+  p.kv_off = N_k - N_q;
+  p.n_qb = (N_q + kBlockRows - 1) / kBlockRows;
+  p.n_kv_tiles = (N_k + kTileN - 1) / kTileN;
+  p.c = scale * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  const long long blocks = (long long)B * H_q * p.n_qb;
+  // causal blocks see on average about half the key tiles
+  const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
+  p.splits = choose_splits(blocks, kv_eff, num_sms());
+  const long long units = blocks * p.splits;
+  if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
+      !make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
+      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  void* ws = nullptr;
+  if (p.splits > 1) {
+    const size_t n_rows = (size_t)units * kBlockRows;
+    const size_t bytes_o = n_rows * d * 4, bytes_ml = n_rows * 8, bytes_c = (size_t)blocks * 4;
+    cudaError_t e = cudaMallocAsync(&ws, bytes_o + bytes_ml + bytes_c, strm);
+    if (e != cudaSuccess) {
+      g_last_cuda_error = (int)e;
+      return FA_ERR_NO_MEMORY;
+    }
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_o);
+    p.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + bytes_o + bytes_ml);
+    e = cudaMemsetAsync(p.counters, 0, bytes_c, strm);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ws, strm);
+      return cuda_fail(e);
+    }
+  }
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)units, strm);
+  if (ws) cudaFreeAsync(ws, strm);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  const Shape s{B, H_q, H_kv, N_q, N_k, d};
+  int st = validate(q, k, v, o, lse, s, scale);
+  if (st != FA_OK) return st;
+  if ((long long)B * H_q * N_q == 0) return FA_OK;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  if (N_k == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
+  const size_t need = fa_naive_workspace_bytes(B, H_q, N_q, N_k);
+  if (!workspace || workspace_bytes < need) return FA_ERR_NO_MEMORY;
+  if (!aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H_q * N_q * d * 2, kb = (size_t)B * H_kv * N_k * d * 2;
+  if (overlaps(workspace, need, q, qb) || overlaps(workspace, need, k, kb) ||
+      overlaps(workspace, need, v, kb) || overlaps(workspace, need, o, qb) ||
+      overlaps(workspace, need, lse, lse ? (size_t)B * H_q * N_q * 4 : 0))
+    return FA_ERR_INVALID_ARG;
+  int* status = device_status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+
+  const int ld = (N_k + 7) / 8 * 8;
+  const int G = H_q / H_kv;
+  CUtensorMap tq, tk, ts, tv;
+  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
+      !make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
+      !make_tmap_bf16_3d(&ts, workspace, ld, N_q, (uint64_t)B * H_q, ld, 128) ||
+      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 64))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  // kernel 1: S = scale * Q K^T  ->  workspace (BF16, rows padded to ld)
+  GemmParams g1{};
+  g1.M = N_q; g1.N = N_k; g1.K = d; g1.batches = B * H_q;
+  g1.heads = H_q; g1.heads_kv = H_kv; g1.group = G;
+  g1.alpha = scale; g1.c = workspace; g1.ldc = ld;
+  cudaError_t e = launch_gemm(false, 128, tq, tk, g1, status, strm);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // kernel 2: P = softmax(S) in place, LSE
+  SoftmaxParams sp{};
+  sp.s = workspace; sp.lse = lse; sp.rows = B * H_q * N_q; sp.n_q = N_q; sp.n_k = N_k; sp.ld = ld;
+  sp.causal = causal ? 1 : 0; sp.kv_off = N_k - N_q;
+  e = launch_row_softmax(sp, strm);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // kernel 3: O = P V
+  GemmParams g3{};
+  g3.M = N_q; g3.N = d; g3.K = ld; g3.batches = B * H_q;
+  g3.heads = H_q; g3.heads_kv = H_kv; g3.group = G;
+  g3.alpha = 1.f; g3.c = o; g3.ldc = d;
+  e = launch_gemm(true, d, ts, tv, g3, status, strm);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

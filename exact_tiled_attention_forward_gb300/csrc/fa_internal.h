@@ -1,0 +1,69 @@
+// Internal launch interface between the C ABI (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+// ---- fused prefill forward ------------------------------------------------------
+constexpr int kTileM = 128;          // query rows per tile (one tcgen05 M=128 MMA)
+constexpr int kTileN = 128;          // keys per K/V tile
+constexpr int kBlockRows = 2 * kTileM;  // query rows per CTA work unit (two ping-pong tiles)
+
+struct FwdParams {
+  int B, H_q, H_kv, N_q, N_k;
+  int causal;
+  int kv_off;       // N_k - N_q: query i sees key j iff j <= i + kv_off (causal)
+  int n_qb;         // query blocks of kBlockRows rows per (b, h)
+  int n_kv_tiles;   // ceil(N_k / kTileN)
+  int splits;       // key-range splits per query block (1 = no merge)
+  float c;          // scale * log2(e)
+  void* o;          // bf16 [B][H_q][N_q][d]
+  float* lse;       // fp32 [B][H_q][N_q] or nullptr
+  float* part_o;    // fp32 [units][kBlockRows][d]        (splits > 1)
+  float* part_ml;   // fp32 [units][kBlockRows][2] (m, l)  (splits > 1)
+  int* counters;    // int  [B*H_q*n_qb], zeroed           (splits > 1)
+  int* status;      // device status word
+};
+
+// Shared-memory bytes the fused kernel needs for head dim d (64 or 128).
+size_t fwd_smem_bytes(int d);
+
+// Launch the fused kernel over `units` = B*H_q*n_qb*splits CTAs.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int units, cudaStream_t stream);
+
+// ---- unfused baseline -------------------------------------------------------------
+struct GemmParams {
+  int M, N, K;          // per batch: C[M][N] = alpha * A[M][K] * B
+  int batches;          // grid z
+  int a_heads_per_b;    // A batch index = z
+  int group;            // B batch index = (z / heads) * heads_kv + (z % heads) / group
+  int heads, heads_kv;
+  float alpha;
+  void* c;              // bf16 output, row stride ldc elements, batch stride M*ldc
+  int ldc;
+};
+cudaError_t launch_gemm(bool b_mn_major, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const GemmParams& p, int* status, cudaStream_t stream);
+size_t gemm_smem_bytes(int bn);
+
+struct SoftmaxParams {
+  void* s;          // bf16 [rows][ld]: scores in, probabilities out (in place)
+  float* lse;       // fp32 [rows] or nullptr
+  int rows, n_q, n_k, ld;
+  int causal, kv_off;
+};
+cudaError_t launch_row_softmax(const SoftmaxParams& p, cudaStream_t stream);
+
+// ---- host helpers -------------------------------------------------------------------
+// 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);
+
+int* device_status_ptr();   // address of the current device's status word (nullptr on error)
+
+}  // namespace fa

@@ -1,0 +1,103 @@
+/* libfa — exact tiled attention forward (FlashAttention forward) for GB300 (sm_103a).
+ *
+ * O = softmax(scale * Q K^T) V, computed tile by tile with an online softmax
+ * (running row max m and running sum l; the partial output is rescaled by
+ * exp(m_old - m_new) when the max rises; O is divided by l once at the end),
+ * so the N_q x N_k score and probability matrices never reach device memory.
+ * Also returned: the FP32 log-sum-exp of each row's scaled scores, the small
+ * per-row statistic the backward pass recomputes from.
+ *
+ * Sources: "Why is standard attention memory-bound, and how does FlashAttention
+ * fix it?" (interview.clozo.ai), Step 1 (definition), Step 3 (online softmax),
+ * Step 4 (saved per-row statistics); "Flash Attention Mechanics: How Tiled
+ * Attention Fits in SRAM" (interviewprepkit.dev), "The Tiling Algorithm";
+ * "FlashAttention HBM bytes, one head, 8K" (inferenceinterviews.com),
+ * "A strong answer" (FA2 query-block order, L2 reuse) and "What interviewers
+ * probe next" (causal tile skipping; decode with GQA).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no reference after the call returns.
+ *  - q: BF16 [B][H_q][N_q][d];  k, v: BF16 [B][H_kv][N_k][d];  o: BF16
+ *    [B][H_q][N_q][d]; lse: FP32 [B][H_q][N_q] or NULL. All contiguous,
+ *    row-major, 16-byte aligned.
+ *  - GQA: query head h reads KV head h / (H_q / H_kv); H_q % H_kv must be 0.
+ *  - causal != 0: query row i sees key j iff j <= i + (N_k - N_q) (bottom-right
+ *    aligned; the usual lower triangle when N_q == N_k). A row that sees no
+ *    key gets O = 0 and LSE = -inf.
+ *  - lse[i] = ln(sum_j exp(scale * q_i . k_j)) over the visible keys.
+ *  - scale must be finite and > 0 (1/sqrt(d) is the usual value).
+ *  - d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ *  - stream: a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous: they return once the work is enqueued. Argument errors are
+ *    reported before anything is enqueued. Launch errors return FA_ERR_CUDA
+ *    (details: fa_get_last_cuda_error). Errors during execution surface at the
+ *    caller's next synchronisation; a kernel that gave up on a bounded wait
+ *    records FA_ERR_TIMEOUT in the device status word (fa_device_status).
+ */
+#ifndef LIBFA_FA_H
+#define LIBFA_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1, /* null/misaligned/overlapping pointer, bad size, H_q % H_kv, scale */
+  FA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (d not 64/128) */
+  FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  FA_ERR_NO_MEMORY = -4,   /* stream-ordered workspace allocation failed, or workspace too small */
+  FA_ERR_TIMEOUT = -5      /* a kernel gave up on a bounded wait (device status word) */
+} fa_status;
+
+/* Exact attention forward, fused (the tiled online-softmax kernel).
+ * Prefill (N_q > 1 or B*H_q large): tcgen05/TMA kernel, two 128-row query
+ * tiles per CTA, K/V tiles of 128 keys. When there are too few query blocks to
+ * fill the GPU, the key range of each block is split over several CTAs and the
+ * partial (m, l, O) results are merged in-kernel. Decode (N_q == 1): split-K
+ * kernel over 256-key chunks with GQA, followed by the same merge.
+ * Split and decode partials live in a stream-ordered workspace
+ * (cudaMallocAsync/cudaFreeAsync on `stream`); nothing outlives the call.
+ * Returns FA_OK or an fa_status code. */
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+               int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream);
+
+/* The unfused three-kernel path, kept as the measured traffic baseline
+ * ("FlashAttention HBM bytes, one head, 8K", "A strong answer": S written,
+ * read, P written, read). Kernel 1: S = scale * Q K^T stored as BF16 in
+ * `workspace`; kernel 2: row softmax S -> P in place (BF16) and LSE; kernel
+ * 3: O = P V. `workspace` is a caller-owned device buffer of at least
+ * fa_naive_workspace_bytes(B, H_q, N_q, N_k) bytes (16-byte aligned); the
+ * score rows are padded to a multiple of 8 elements. Same conventions and
+ * return codes as fa_forward; FA_ERR_NO_MEMORY if workspace_bytes is short. */
+int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_naive_forward needs: B*H_q*N_q*roundup(N_k, 8)*2. 0 on bad sizes. */
+size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k);
+
+/* Static description of an fa_status code. Never NULL. */
+const char* fa_status_string(int status);
+
+/* The cudaError_t of the last CUDA failure this thread saw inside libfa (0 if none). */
+int fa_get_last_cuda_error(void);
+
+/* Synchronises the current device, then returns FA_OK or FA_ERR_TIMEOUT from
+ * the device status word that kernels set when a bounded wait runs out;
+ * `reset` != 0 clears the word afterwards. FA_ERR_CUDA if synchronisation fails. */
+int fa_device_status(int reset);
+
+/* Library version, (major << 16) | minor. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBFA_FA_H */

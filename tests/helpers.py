@@ -1,0 +1,48 @@
+"""Shared helpers for the GPU parity tests (device transfer, tolerance checks)."""
+import numpy as np
+
+import oracle
+
+# Tolerances on BF16 inputs (FP32 accumulate, BF16 output)
+TOL_MAX_ABS_O = 1e-2
+TOL_REL_L2_O = 5e-3
+TOL_MAX_ABS_LSE = 1e-3
+
+
+def to_dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bf16_dev_to_f64(t):
+    import torch
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL_L2_O,
+            tol_lse=TOL_MAX_ABS_LSE):
+    """Element-wise comparison of O and LSE; returns a dict of error figures."""
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    assert o_gpu.shape == o_ref.shape
+    assert np.isfinite(o_gpu).all(), "non-finite values in O"
+    err = np.abs(o_gpu - o_ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    denom = float(np.linalg.norm(o_ref))
+    rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))
+    res = {"max_abs_o": max_abs, "rel_l2_o": rel}
+    if lse_ref is not None:
+        lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
+        inf_ref = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(lse_gpu), inf_ref), "LSE -inf pattern differs"
+        fin = ~inf_ref
+        lerr = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
+        res["max_abs_lse"] = lerr
+        assert lerr <= tol_lse, res
+    assert max_abs <= tol_o, res
+    assert rel <= tol_rel, res
+    return res
+
+
+def run_oracle(a):
+    return oracle.attention_reference(a.q, a.k, a.v, causal=a.causal, scale=a.scale)

@@ -1,0 +1,107 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, validates
+arguments on the host (no device work is started for a rejected call)."""
+import ctypes
+import math
+import os
+import shutil
+
+import pytest
+
+import exact_tiled_attention_forward_gb300 as fa
+from exact_tiled_attention_forward_gb300 import build as fa_build
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="CUDA toolkit not installed")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIB_PATH):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("libfa.so not built and no nvcc")
+        fa_build.build()
+    return fa.lib()
+
+
+def test_header_symbols_exported(lib):
+    names = fa.header_functions()
+    assert set(names) == {"fa_forward", "fa_naive_forward", "fa_naive_workspace_bytes",
+                          "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
+                          "fa_version"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        s = fa.fa_status_string(code)
+        assert isinstance(s, str) and s
+    assert fa.fa_status_string(-5) == "kernel wait timed out"
+    assert fa.fa_version() == (0, 1)
+
+
+def test_workspace_bytes(lib):
+    assert fa.fa_naive_workspace_bytes(1, 1, 8192, 8192) == 8192 * 8192 * 2
+    assert fa.fa_naive_workspace_bytes(2, 3, 5, 9) == 2 * 3 * 5 * 16 * 2   # rows padded to 8
+    assert fa.fa_naive_workspace_bytes(-1, 1, 1, 1) == 0
+
+
+# fake, 16-byte aligned, non-overlapping addresses: validation never dereferences them
+Q, K, V, O, L = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def _fwd(lib, q=Q, k=K, v=V, o=O, l=L, B=1, Hq=2, Hkv=1, Nq=64, Nk=64, d=128, causal=0,
+         scale=0.125):
+    return lib.fa_forward(q, k, v, o, l, B, Hq, Hkv, Nq, Nk, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=3, Hkv=2), fa.FA_ERR_INVALID_ARG),            # H_q % H_kv != 0
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),                    # null q
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q=Q + 8), fa.FA_ERR_INVALID_ARG),                # misaligned
+    (dict(l=L + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(o=Q + 64), fa.FA_ERR_INVALID_ARG),               # o overlaps q
+    (dict(o=V), fa.FA_ERR_INVALID_ARG),                    # o aliases v
+    (dict(l=O + 16), fa.FA_ERR_INVALID_ARG),               # lse inside o
+    (dict(B=1 << 16, Hq=1 << 8, Hkv=1, Nq=1 << 8), fa.FA_ERR_INVALID_ARG),  # > 2^31 rows
+])
+def test_forward_rejects(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+
+
+def test_empty_query_is_a_no_op(lib):
+    # nothing to write: success without touching the device (null pointers allowed)
+    assert _fwd(lib, q=0, k=0, v=0, o=0, l=0, Nq=0) == fa.FA_OK
+    assert _fwd(lib, q=0, k=0, v=0, o=0, l=0, B=0) == fa.FA_OK
+
+
+def test_naive_rejects(lib):
+    f = lib.fa_naive_forward
+    need = lib.fa_naive_workspace_bytes(1, 2, 64, 64)
+    W = 0x60000000
+    assert f(Q, K, V, O, L, 1, 3, 2, 64, 64, 128, 0, 0.1, W, need, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.1, W, need - 1, None) == fa.FA_ERR_NO_MEMORY
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, need, None) == fa.FA_ERR_NO_MEMORY
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.1, W + 8, need, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.1, O - 16, need, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 80, 0, 0.1, W, need, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_no_gpu_fails_loudly(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    # a valid request on a machine without a GPU is a CUDA error, never a silent success
+    assert _fwd(lib) == fa.FA_ERR_CUDA

@@ -1,0 +1,145 @@
+"""GPU parity: libfa's fused forward (through the C ABI) against the FP64 oracle,
+element by element, on seeded inputs; plus edge cases and determinism."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_forward_gb300 import inputs as I
+
+from helpers import compare, to_dev, bf16_dev_to_f64, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import exact_tiled_attention_forward_gb300 as fa
+    from exact_tiled_attention_forward_gb300 import build
+    build.build()
+    fa.lib()
+    return fa
+
+
+def _run(fa, a, naive=False):
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    fn = fa.fa_naive_forward if naive else fa.fa_forward
+    o, lse = fn(q, k, v, causal=a.causal, scale=a.scale)
+    import torch
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    return bf16_dev_to_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+SMALL = [
+    # (B, H_q, H_kv, N_q, N_k, d, causal)
+    (1, 1, 1, 1, 1, 64, False),
+    (1, 1, 1, 17, 17, 128, True),
+    (1, 1, 1, 127, 127, 64, False),
+    (1, 1, 1, 128, 128, 128, True),
+    (1, 1, 1, 129, 129, 128, False),
+    (1, 2, 1, 255, 255, 64, True),
+    (1, 1, 1, 256, 256, 128, True),
+    (1, 1, 1, 257, 257, 128, True),
+    (2, 2, 2, 383, 383, 64, True),
+    (1, 3, 3, 513, 513, 128, False),
+    (2, 8, 2, 300, 700, 128, True),     # GQA, N_q < N_k
+    (2, 8, 2, 300, 700, 128, False),
+    (1, 4, 4, 600, 200, 64, True),      # N_q > N_k: leading rows see no key
+    (1, 2, 1, 1000, 1000, 128, False),
+    (3, 4, 1, 64, 1000, 128, False),    # GQA group 4
+    (1, 1, 1, 1, 5000, 128, False),     # one query row, long key range
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:6])) + ("c" if s[6] else ""))
+def test_small_shapes(fa, shape):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=1)
+    o, lse = _run(fa, a)
+    o_ref, lse_ref = run_oracle(a)
+    compare(o, lse, o_ref, lse_ref)
+
+
+def test_tiny_workload_n256_d64(fa):
+    a = I.make_workload("tiny_n256_d64")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
+def test_one_head_n8192_d128(fa):
+    # the split-key path: 32 query blocks are too few for the GPU, so each block's
+    # key range is split over several CTAs and merged in-kernel
+    a = I.make_workload("one_head_n8192_d128")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
+@pytest.mark.parametrize("name", ["h32_n4096_d128", "h32_n4096_d128_causal"])
+def test_h32_n4096(fa, name):
+    a = I.make_workload(name)
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
+def test_decode_b16_h32_kv8(fa):
+    a = I.make_workload("decode_b16_h32_kv8_n8192_d128")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
+def test_deterministic(fa):
+    a = I.make_inputs(1, 2, 1, 1000, 1500, 128, causal=True, seed=4, k_row_frac=0.01)
+    o1, l1 = _run(fa, a)
+    o2, l2 = _run(fa, a)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_empty_keys_and_queries(fa):
+    import torch
+    q = torch.randn(1, 2, 5, 128, device="cuda").bfloat16()
+    k = torch.empty(1, 1, 0, 128, device="cuda", dtype=torch.bfloat16)
+    o, lse = fa.fa_forward(q, k, k)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    q0 = torch.empty(1, 2, 0, 128, device="cuda", dtype=torch.bfloat16)
+    o0, l0 = fa.fa_forward(q0, q, q)
+    assert o0.numel() == 0
+
+
+def naive_lse_bound(a):
+    """Per-row LSE tolerance of the unfused path: it stores S in BF16, so each
+    score carries a relative rounding error up to u = 2^-8, and
+    |dLSE_i| = |sum_j p_ij dS_ij| <= u * max_j |s_ij| <= u * scale * |q_i| * max_j |k_j|."""
+    from oracle.attention import bf16_to_f64
+    qf, kf = bf16_to_f64(a.q), bf16_to_f64(a.k)
+    g = a.H_q // a.H_kv
+    kmax = np.repeat(np.linalg.norm(kf, axis=-1).max(-1), g, axis=1)     # [B, H_q]
+    return 2.0 ** -8 * a.scale * np.linalg.norm(qf, axis=-1) * kmax[..., None] + 1e-4
+
+
+def test_naive_matches_oracle(fa):
+    # O: BF16 P adds a relative error <= 2^-8 per weight on top of the score rounding;
+    # the bound used is twice the fused path's (max|dO| <= 2e-2, rel L2 <= 1e-2).
+    for shape in [(1, 1, 1, 256, 256, 64, False), (1, 2, 1, 300, 517, 128, True),
+                  (2, 4, 2, 129, 129, 128, False)]:
+        a = I.make_inputs(*shape[:6], causal=shape[6], seed=2)
+        o, lse = _run(fa, a, naive=True)
+        o_ref, lse_ref = run_oracle(a)
+        compare(o, None, o_ref, None, tol_o=2e-2, tol_rel=1e-2)
+        bound = naive_lse_bound(a)
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isneginf(lse), ~fin)
+        assert np.all(np.abs(lse - lse_ref)[fin] <= bound[fin])
+
+
+def test_naive_one_head_n8192(fa):
+    a = I.make_workload("one_head_n8192_d128")
+    o, lse = _run(fa, a, naive=True)
+    o_ref, lse_ref = run_oracle(a)
+    compare(o, None, o_ref, None, tol_o=2e-2, tol_rel=1e-2)
+    assert np.all(np.abs(lse - lse_ref) <= naive_lse_bound(a))
