@@ -1,0 +1,442 @@
+"""Benchmark of the exact attention forward on GB300 (one JSON line on rank 0).
+
+Default workload: one head, N_q = N_k = 8192, d = 128, non-causal, BF16
+Q/K/V ~ N(0, 1), scale 1/sqrt(d) (34.4 GFLOP per step). A step is one
+``fa_forward`` call through the C ABI over that batch. The inputs (8 MiB)
+fit in L2, so L2 is flushed (256 MiB write) before every timed step, outside
+the step's CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fused|naive|reference]
+                    [--workload NAME]
+
+``--impl reference`` times the FP64 CPU oracle on the host cores (the only
+other place this file runs the oracle besides the ``cpu_baseline`` leg).
+Under torchrun (N > 1) every rank runs one independent replica of the
+workload (the path needs no exchange between GPUs); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import numpy as np  # noqa: E402
+
+from exact_tiled_attention_forward_gb300 import inputs as I  # noqa: E402
+from exact_tiled_attention_forward_gb300 import work as W  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofline"
+DEFAULT_WORKLOAD = "one_head_n8192_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
+                  "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None if there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    m_h = re.search(r"^kernel_source_sha256_16:\s*([0-9a-f]+)", text, re.M)
+    if not m_b or not m_h or m_h.group(1) != kernel_hash():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """SM clock and throttle-reason samples taken DURING the timed region.
+
+    Reads NVML (libnvidia-ml, through ctypes) every 2 ms from a thread, so even
+    a timed region of a few milliseconds gets samples; falls back to
+    ``nvidia-smi -lms 200`` if NVML cannot be loaded. Read-only: no setting of
+    the GPU is changed.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, bus_id: str | None, uuid: str | None):
+        self.bus_id, self.uuid = bus_id, uuid
+        self.samples, self.reason_bits, self.max_mhz = [], 0, None
+        self.nvml = self.dev = None
+        self.thread = None
+        self.smi = None
+        self._stop = False
+
+    def _open_nvml(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        dev = ctypes.c_void_p()
+        ok = False
+        if self.bus_id:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(self.bus_id.encode(), ctypes.byref(dev)) == 0
+        if not ok and self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(dev)) == 0
+        if not ok:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self.nvml, self.dev = lib, dev
+        return True
+
+    def _loop(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_r = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop:
+            if self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if get_r(self.dev, ctypes.byref(rs)) == 0:
+                self.reason_bits |= int(rs.value)
+            time.sleep(0.002)
+
+    def start(self):
+        try:
+            have = self._open_nvml()
+        except Exception:  # noqa: BLE001 - any NVML trouble falls back to nvidia-smi
+            have = False
+        if have:
+            import threading
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            return
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.smi = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=pci.bus_id,clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.smi = None
+
+    def stop(self):
+        if self.thread is not None:
+            self._stop = True
+            self.thread.join()
+            src = "nvml, 2 ms"
+        elif self.smi is not None:
+            self.smi.terminate()
+            self.smi.wait(timeout=5)
+            self.out.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+                    "sw_power_cap": 0x4}
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 7 or (self.bus_id and self.bus_id[-12:].lower() not in parts[0].lower()):
+                    continue
+                try:
+                    self.samples.append(float(parts[1]))
+                    self.max_mhz = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[3:7]):
+                    if val.lower() == "active":
+                        self.reason_bits |= bits[nm]
+            os.unlink(self.path)
+            src = "nvidia-smi, 200 ms"
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["unavailable"]}
+        reasons = sorted(v for b, v in self.REASONS.items() if self.reason_bits & b)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": reasons,
+                "source": src}
+
+
+def workload_config(name: str):
+    cfg = dict(I.WORKLOADS[name])
+    a_flops = W.flops_pages(cfg["B"], cfg["H_q"], cfg["N_q"], cfg["N_k"], cfg["d"], cfg["causal"])
+    a_bytes = W.bytes_moved(cfg["B"], cfg["H_q"], cfg["H_kv"], cfg["N_q"], cfg["N_k"], cfg["d"])
+    decode = cfg["N_q"] == 1
+    return cfg, a_flops, a_bytes, decode
+
+
+def cpu_oracle_throughput(a, budget_s: float, max_rows: int | None = None):
+    """Time the oracle on the host over query rows taken head by head (whole
+    heads, or the first rows of each head once ``max_rows`` is reached), until
+    ``budget_s`` has elapsed or ``max_rows`` rows are done.
+
+    Returns (rows done, seconds, threads used, (batch, head) calls)."""
+    import oracle
+    B, Hq, Hkv, Nq, Nk, d = a.shape_args
+    t0 = time.perf_counter()
+    done_rows = 0
+    calls = 0
+    while True:
+        for b in range(B):
+            for h in range(Hq):
+                n = Nq if max_rows is None else min(Nq, max_rows - done_rows)
+                if n <= 0:
+                    break
+                oracle.attention_rows(a.q, a.k, a.v, b, h, np.arange(n), causal=a.causal,
+                                      scale=a.scale)
+                done_rows += n
+                calls += 1
+                if time.perf_counter() - t0 >= budget_s and max_rows is None:
+                    break
+            else:
+                continue
+            break
+        if max_rows is not None or time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return done_rows, dt, cores, calls
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fused", choices=["fused", "naive", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of host time for the cpu_baseline leg (0 disables it)")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    cfg, a_flops, a_bytes, decode = workload_config(args.workload)
+    unit = "GB/s" if decode else "TFLOP/s"
+    work_per_step = (a_bytes / 1e9) if decode else (a_flops / 1e12)
+
+    if args.impl == "reference":
+        # The oracle on the host cores, rank 0 only; other ranks exit without work.
+        if rank != 0:
+            return
+        a = I.make_workload(args.workload)
+        B, Hq = cfg["B"], cfg["H_q"]
+        rows_sample = min(B * Hq * cfg["N_q"], 2048)
+        per_row = work_per_step / (B * Hq * cfg["N_q"])
+        for _ in range(warmup):
+            cpu_oracle_throughput(a, 0.0, rows_sample)
+        times = []
+        for _ in range(args.steps):
+            n_rows, dt, cores, _ = cpu_oracle_throughput(a, 0.0, rows_sample)
+            times.append(dt / n_rows)
+        t_row = statistics.mean(times)
+        value = per_row / t_row
+        sample = (f"{rows_sample} query rows per step, taken head by head "
+                  f"(of {B * Hq * cfg['N_q']} rows in the workload)")
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
+                "ms_per_step": t_row * rows_sample * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, **cfg},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import exact_tiled_attention_forward_gb300 as fa
+
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    fa.lib()
+
+    a = I.make_workload(args.workload)
+    B, Hq, Hkv, Nq, Nk, d = a.shape_args
+
+    def to_dev(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    o = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    fn = fa.fa_forward if args.impl == "fused" else fa.fa_naive_forward
+    ws = None
+    if args.impl == "naive":
+        ws = torch.empty(fa.fa_naive_workspace_bytes(B, Hq, Nq, Nk), dtype=torch.uint8, device=dev)
+    kernels_per_step = 3 if args.impl == "naive" else 1
+
+    def step(qq=q, kk=k, vv=v):
+        if ws is None:
+            fn(qq, kk, vv, causal=a.causal, scale=a.scale, out=o, lse=lse)
+        else:
+            fn(qq, kk, vv, causal=a.causal, scale=a.scale, out=o, lse=lse, workspace=ws)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    barrier()
+
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    bus_id = None
+    if bus is not None:
+        bus_id = (f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:"
+                  f"{getattr(props, 'pci_device_id', 0):02x}.0")
+    uuid = getattr(props, "uuid", None)
+    uuid = None if uuid is None else ("GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid))
+    sampler = ClockSampler(bus_id, uuid)
+    sampler.start()
+    # ---- timed region: K steps, each bracketed by its own events; L2 flushed between
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * work_per_step * args.steps / (total_ms * 1e-3)
+    if fa.fa_device_status() != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait during the benchmark")
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hq, hk, hv = pin(a.q), pin(a.k), pin(a.v)
+    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step(dq, dk, dv)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    barrier()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for e0, e1 in eev:
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+    barrier()
+    e2e_ms = sum(e0.elapsed_time(e1) for e0, e1 in eev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * work_per_step * args.steps / (e2e_ms * 1e-3)
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    if decode:
+        peak = float(peaks["hbm_gbs"])
+        achieved = a_bytes / 1e9 / (ms_per_step * 1e-3)
+        roof = {"bound": "hbm", "unit": "GB/s"}
+    else:
+        peak = float(peaks["bf16_tflops"])
+        achieved = a_flops / 1e12 / (ms_per_step * 1e-3)
+        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+    traffic = profiled_traffic(args.workload) if args.impl == "fused" else None
+    roof.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
+                 "traffic": traffic, "peak_source": f"{peak_src} (burst)",
+                 "algorithmic_per_launch": a_bytes if decode else a_flops,
+                 "kernel": "fa_fwd_kernel" if args.impl == "fused" else "naive (3 kernels)"})
+
+    cpu = None
+    if args.cpu_budget > 0 and world == 1:
+        per_row = work_per_step / (B * Hq * Nq)
+        n_rows, dt, cores, calls = cpu_oracle_throughput(a, args.cpu_budget)
+        cpu = {"value": per_row * n_rows / dt, "unit": unit, "cores": cores, "kind": "oracle",
+               "sample": f"{n_rows} query rows ({calls} heads x {Nq} rows) in {dt:.1f} s, "
+                         f"FP64 materialised oracle, numpy/OpenBLAS"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "impl": args.impl,
+        "config": {"workload": args.workload, **{k2: cfg[k2] for k2 in
+                   ("B", "H_q", "H_kv", "N_q", "N_k", "d", "causal")},
+                   "scale": a.scale, "l2": "flushed before every step (256 MiB write, outside events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -96,6 +96,30 @@ int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st) {
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+// Library-owned stream-ordered pool for split/decode partials, one per device.
+// Its release threshold is the maximum, so memory freed at the end of one call
+// stays reserved for the next instead of going back to the driver at every
+// synchronisation (which would make each call pay a fresh physical allocation).
+cudaMemPool_t workspace_pool() {
+  static cudaMemPool_t pools[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t thr = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -234,7 +258,9 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   if (p.splits > 1) {
     const size_t n_rows = (size_t)units * kBlockRows;
     const size_t bytes_o = n_rows * d * 4, bytes_ml = n_rows * 8, bytes_c = (size_t)blocks * 4;
-    cudaError_t e = cudaMallocAsync(&ws, bytes_o + bytes_ml + bytes_c, strm);
+    cudaMemPool_t pool = workspace_pool();
+    if (!pool) return cuda_fail(cudaGetLastError());
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes_o + bytes_ml + bytes_c, pool, strm);
     if (e != cudaSuccess) {
       g_last_cuda_error = (int)e;
       return FA_ERR_NO_MEMORY;

@@ -61,8 +61,10 @@ typedef enum {
  * fill the GPU, the key range of each block is split over several CTAs and the
  * partial (m, l, O) results are merged in-kernel. Decode (N_q == 1): split-K
  * kernel over 256-key chunks with GQA, followed by the same merge.
- * Split and decode partials live in a stream-ordered workspace
- * (cudaMallocAsync/cudaFreeAsync on `stream`); nothing outlives the call.
+ * Split and decode partials live in a stream-ordered workspace taken from a
+ * library-owned memory pool on the current device (cudaMallocFromPoolAsync /
+ * cudaFreeAsync on `stream`); the pool keeps freed memory reserved for later
+ * calls until the process exits. No pointer outlives the call.
  * Returns FA_OK or an fa_status code. */
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream);
