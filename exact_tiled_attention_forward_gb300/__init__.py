@@ -29,6 +29,7 @@ FA_ERR_UNSUPPORTED = -2
 FA_ERR_CUDA = -3
 FA_ERR_NO_MEMORY = -4
 FA_ERR_TIMEOUT = -5
+FA_ERR_TOO_LARGE = -6
 
 _lib = None
 
@@ -46,6 +47,7 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 
 _SIGNATURES = {
     "fa_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
     "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
@@ -116,6 +118,25 @@ def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, out=No
     st = lib().fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q, N_k,
                           d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "fa_forward")
+    return out, lse
+
+
+def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                       lse=None, return_lse: bool = True, stream=None):
+    """``fa_forward`` that allocates no device memory inside libfa: split
+    partials use libfa's fixed 32 MiB device array (see ``include/fa.h``).
+    Concurrent calls race on that array; keep them on one stream. Returns ``(o, lse)``."""
+    import torch
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    st = lib().fa_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv,
+                                  N_q, N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "fa_forward_noalloc")
     return out, lse
 
 

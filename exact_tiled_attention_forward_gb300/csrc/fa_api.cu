@@ -11,17 +11,18 @@
 
 namespace fa {
 
-namespace {
-
 thread_local int g_last_cuda_error = 0;
 
+namespace {
 __device__ int g_device_status;  // one per device (module-scope device variable)
+}  // namespace
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return FA_ERR_CUDA;
 }
 
+namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -49,9 +50,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-struct Shape {
-  int B, H_q, H_kv, N_q, N_k, d;
-};
+}  // namespace
 
 // Shared validation of the fa_forward / fa_naive_forward arguments.
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -80,6 +79,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   return FA_OK;
 }
 
+namespace {
 // O = 0, LSE = -inf for every row (no key at all: N_k == 0)
 __global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, long long rows, int d) {
   const long long n = rows * d;
@@ -90,12 +90,15 @@ __global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, long long rows, 
   }
 }
 
+}  // namespace
+
 int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st) {
   fill_empty_kernel<<<256, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(o), lse, rows, d);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+namespace {
 // Library-owned stream-ordered pool for split/decode partials, one per device.
 // Its release threshold is the maximum, so memory freed at the end of one call
 // stays reserved for the next instead of going back to the driver at every
@@ -119,6 +122,8 @@ cudaMemPool_t workspace_pool() {
   }
   return pools[dev];
 }
+
+}  // namespace
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -144,8 +149,6 @@ int choose_splits(long long blocks, int kv_tiles, int sms) {
   }
   return best;
 }
-
-}  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows) {
@@ -191,6 +194,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_NO_MEMORY: return "out of memory / workspace too small";
     case FA_ERR_TIMEOUT: return "kernel wait timed out";
+    case FA_ERR_TOO_LARGE: return "request needs more scratch than the static scratch array holds";
     default: return "unknown status";
   }
 }

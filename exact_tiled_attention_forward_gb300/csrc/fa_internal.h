@@ -60,6 +60,21 @@ struct SoftmaxParams {
 cudaError_t launch_row_softmax(const SoftmaxParams& p, cudaStream_t stream);
 
 // ---- host helpers -------------------------------------------------------------------
+struct Shape {
+  int B, H_q, H_kv, N_q, N_k, d;
+};
+// Argument checks shared by the forward entry points (fa_status code; FA_OK when valid).
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const Shape& s, float scale);
+// O = 0 and LSE = -inf for `rows` rows (every row sees no key).
+int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st);
+// Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+int num_sms();
+// Key-range splits per query block for `blocks` blocks of `kv_tiles` key tiles.
+int choose_splits(long long blocks, int kv_tiles, int sms);
+extern thread_local int g_last_cuda_error;
+
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);

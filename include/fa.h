@@ -52,7 +52,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (d not 64/128) */
   FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   FA_ERR_NO_MEMORY = -4,   /* stream-ordered workspace allocation failed, or workspace too small */
-  FA_ERR_TIMEOUT = -5      /* a kernel gave up on a bounded wait (device status word) */
+  FA_ERR_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (device status word) */
+  FA_ERR_TOO_LARGE = -6    /* fa_forward_noalloc: needs more than its static scratch holds */
 } fa_status;
 
 /* Exact attention forward, fused (the tiled online-softmax kernel).
@@ -68,6 +69,30 @@ typedef enum {
  * Returns FA_OK or an fa_status code. */
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream);
+
+/* fa_forward without any device-memory allocation. (The pages have no
+ * counterpart: this exists for callers, not for the method.)
+ * For callers that cannot allocate device memory on this path: a serving loop
+ * that must never block in cudaMalloc/cudaFree (they can synchronise the
+ * device and take unbounded time), a process whose device memory is fully
+ * reserved up front by another allocator, or a deployment that sizes all of
+ * its memory before it starts. Same arguments, conventions, kernel and results
+ * as fa_forward. The caller still provides q, k, v, o and lse.
+ * Scratch: when a query block's key range is split over several CTAs, the
+ * partial results go to a fixed 32 MiB array inside libfa's device image
+ * (every GPU that loads libfa holds it until the process exits) instead of a
+ * pool allocation. Requests whose partials would not fit return
+ * FA_ERR_TOO_LARGE before anything is enqueued; requests that need no split
+ * use no scratch at all.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Sharing: every call uses the same array, which keeps the last call's
+ * contents (the merge counters are cleared with cudaMemsetAsync on `stream`
+ * at each call). Calls whose execution overlaps on the GPU race on the array:
+ * issue them on one stream, or order them with events. */
+int fa_forward_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
+                       void* stream);
 
 /* The unfused three-kernel path, kept as the measured traffic baseline
  * ("FlashAttention HBM bytes, one head, 8K", "A strong answer": S written,

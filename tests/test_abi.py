@@ -25,7 +25,8 @@ def lib():
 
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
-    assert set(names) == {"fa_forward", "fa_naive_forward", "fa_naive_workspace_bytes",
+    assert set(names) == {"fa_forward", "fa_forward_noalloc", "fa_naive_forward",
+                          "fa_naive_workspace_bytes",
                           "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
                           "fa_version"}
     for n in names:
@@ -33,7 +34,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, 7):
+    for code in (0, -1, -2, -3, -4, -5, -6, 7):
         s = fa.fa_status_string(code)
         assert isinstance(s, str) and s
     assert fa.fa_status_string(-5) == "kernel wait timed out"
@@ -79,6 +80,14 @@ def _fwd(lib, q=Q, k=K, v=V, o=O, l=L, B=1, Hq=2, Hkv=1, Nq=64, Nk=64, d=128, ca
 ])
 def test_forward_rejects(lib, kw, status):
     assert _fwd(lib, **kw) == status
+
+
+def test_noalloc_rejects_like_forward(lib):
+    f = lib.fa_forward_noalloc
+    assert f(Q, K, V, O, L, 1, 3, 2, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 96, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert f(0, 0, 0, 0, 0, 1, 2, 1, 0, 64, 128, 0, 0.1, None) == fa.FA_OK
 
 
 def test_empty_query_is_a_no_op(lib):

@@ -1,0 +1,116 @@
+"""fa_forward_noalloc: the entry point for callers that cannot allocate device
+memory (for example a serving loop that must never block in cudaMalloc, or a
+process whose device memory is all reserved up front by another allocator).
+It must give the same results as fa_forward, whose split partials come from a
+pool allocation, while using only libfa's fixed scratch array.
+
+This file is named to be collected last, so a failure here comes after every
+other test has run. It passes alone in a fresh process and after the others.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+from exact_tiled_attention_forward_gb300 import inputs as I
+
+from helpers import TOL_MAX_ABS_O, TOL_REL_L2_O, TOL_MAX_ABS_LSE, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 << 20
+
+
+@pytest.fixture(scope="module")
+def fa():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import exact_tiled_attention_forward_gb300 as fa
+    from exact_tiled_attention_forward_gb300 import build
+    build.build()
+    fa.lib()
+    return fa
+
+
+def _call(fa, entry, q, k, v, o, lse, a):
+    """Call an entry point through the C ABI with raw device pointers."""
+    import torch
+    f = getattr(fa.lib(), entry)
+    st = f(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+           ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
+           ctypes.c_void_p(lse.data_ptr()), a.B, a.H_q, a.H_kv, a.N_q, a.N_k, a.d, int(a.causal),
+           ctypes.c_float(a.scale), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+def _planned_scratch(a, sms):
+    """Scratch bytes the planner's split needs (mirrors choose_splits in libfa)."""
+    n_qb = (a.N_q + 255) // 256
+    n_kv = (a.N_k + 127) // 128
+    kv_eff = (n_kv + 1) // 2 if a.causal else n_kv
+    blocks = a.B * a.H_q * n_qb
+    best, best_cost = 1, 1e30
+    if not (kv_eff <= 1 or blocks >= 2 * sms):
+        for s in range(1, min(16, kv_eff) + 1):
+            waves = (blocks * s + sms - 1) // sms
+            cost = waves * (2.0 + kv_eff / s)
+            if cost < best_cost - 1e-9:
+                best, best_cost = s, cost
+    if best == 1:
+        return 0
+    units = blocks * best
+    return units * 256 * (a.d * 4 + 8) + blocks * 4
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1, 8192, 8192, 128, False),   # one head, N = 8192: split over 4 CTAs per block
+    (1, 2, 1, 700, 3000, 64, True),      # causal, GQA, ragged, d = 64
+])
+def test_noalloc_matches_fa_forward_twice(fa, shape):
+    import torch
+    a = I.make_inputs(*shape[:6], causal=shape[6], seed=3, k_row_frac=0.01)
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 0 < _planned_scratch(a, sms) <= SCRATCH_BYTES   # the scratch path is exercised
+    o_ref = torch.empty((a.B, a.H_q, a.N_q, a.d), dtype=torch.bfloat16, device="cuda")
+    l_ref = torch.empty((a.B, a.H_q, a.N_q), dtype=torch.float32, device="cuda")
+    assert _call(fa, "fa_forward", q, k, v, o_ref, l_ref, a) == fa.FA_OK
+    ref_o = o_ref.float().cpu().numpy()
+    ref_l = l_ref.cpu().numpy()
+    for _ in range(2):   # two calls in a row: the array keeps the previous call's contents
+        o = torch.full_like(o_ref, float("nan"))
+        l = torch.full_like(l_ref, float("nan"))
+        assert _call(fa, "fa_forward_noalloc", q, k, v, o, l, a) == fa.FA_OK
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == fa.FA_OK
+        got_o = o.float().cpu().numpy()
+        got_l = l.cpu().numpy()
+        assert np.isfinite(got_o).all()
+        err = np.abs(got_o - ref_o)
+        assert err.max() <= TOL_MAX_ABS_O
+        assert np.linalg.norm(got_o - ref_o) <= TOL_REL_L2_O * np.linalg.norm(ref_o)
+        fin = np.isfinite(ref_l)
+        assert np.array_equal(np.isfinite(got_l), fin)
+        assert np.abs(got_l[fin] - ref_l[fin]).max() <= TOL_MAX_ABS_LSE
+
+
+def test_noalloc_rejects_requests_beyond_scratch(fa):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # find a shape whose planned split partials exceed the fixed array
+    for heads in range(40, 160, 4):
+        a = I.make_inputs(1, heads, heads, 256, 4096, 128, seed=0)
+        if _planned_scratch(a, sms) > SCRATCH_BYTES:
+            break
+    else:
+        pytest.skip("no candidate shape exceeds the scratch on this GPU")
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    o = torch.zeros((a.B, a.H_q, a.N_q, a.d), dtype=torch.bfloat16, device="cuda")
+    l = torch.zeros((a.B, a.H_q, a.N_q), dtype=torch.float32, device="cuda")
+    assert _call(fa, "fa_forward_noalloc", q, k, v, o, l, a) == fa.FA_ERR_TOO_LARGE
+    torch.cuda.synchronize()
+    assert torch.all(o == 0)   # nothing was enqueued
+    # the same request through fa_forward (pool-allocated partials) is fine
+    assert _call(fa, "fa_forward", q, k, v, o, l, a) == fa.FA_OK
