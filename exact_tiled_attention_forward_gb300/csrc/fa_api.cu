@@ -132,22 +132,45 @@ int num_sms() {
   return n;
 }
 
-// Splits per query block when there are too few blocks to fill the GPU.
-// Cost model: waves * (2 + tiles per split), in units of one K/V tile step.
-int choose_splits(long long blocks, int kv_tiles, int sms) {
-  if (kv_tiles <= 1 || blocks >= 2ll * sms) return 1;
+// Cut the query blocks into CTAs. Whole blocks fill complete waves of the
+// GPU; the blocks of an incomplete last wave (all blocks, when there are fewer
+// than one wave) have their key range split into s parts when that shortens
+// the tail, and a merge kernel combines the parts. Cost model, in key-tile
+// steps: waves * (2 + key tiles per part) + 0.5 for the merge. Causal
+// problems with at least a wave of blocks are not split: their blocks differ
+// in length and the in-order dispatch of longest-first blocks balances them.
+FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms) {
+  FwdPlan pl{};
+  pl.u_full = (int)blocks;
+  pl.n_tail = 0;
+  pl.s_tail = 1;
+  pl.units = blocks;
+  pl.part_bytes = 0;
+  if (blocks <= 0 || kv_tiles <= 1 || sms <= 0) return pl;
+  long long tail = 0;
+  if (blocks < sms) {
+    tail = blocks;
+  } else if (!causal) {
+    tail = blocks % sms;
+  }
+  if (tail == 0) return pl;
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= 16 && s <= kv_tiles; ++s) {
-    const long long units = blocks * s;
-    const long long waves = (units + sms - 1) / sms;
-    const double cost = (double)waves * (2.0 + (double)kv_tiles / s);
+    const long long waves = (tail * s + sms - 1) / sms;
+    const double cost = (double)waves * (2.0 + (double)kv_tiles / s) + (s > 1 ? 0.5 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
   }
-  return best;
+  if (best == 1) return pl;
+  pl.u_full = (int)(blocks - tail);
+  pl.n_tail = (int)tail;
+  pl.s_tail = best;
+  pl.units = (blocks - tail) + tail * best;
+  pl.part_bytes = (size_t)tail * best * kBlockRows * ((size_t)d * 4 + 8);
+  return pl;
 }
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
@@ -248,9 +271,12 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   const long long blocks = (long long)B * H_q * p.n_qb;
   // causal blocks see on average about half the key tiles
   const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
-  p.splits = choose_splits(blocks, kv_eff, num_sms());
-  const long long units = blocks * p.splits;
-  if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
+  if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  p.u_full = pl.u_full;
+  p.n_tail = pl.n_tail;
+  p.s_tail = pl.s_tail;
+  const long long units = pl.units;
 
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
@@ -259,24 +285,17 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
     return cuda_fail(cudaErrorInvalidValue);
 
   void* ws = nullptr;
-  if (p.splits > 1) {
-    const size_t n_rows = (size_t)units * kBlockRows;
-    const size_t bytes_o = n_rows * d * 4, bytes_ml = n_rows * 8, bytes_c = (size_t)blocks * 4;
+  if (pl.n_tail > 0) {
     cudaMemPool_t pool = workspace_pool();
     if (!pool) return cuda_fail(cudaGetLastError());
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes_o + bytes_ml + bytes_c, pool, strm);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.part_bytes, pool, strm);
     if (e != cudaSuccess) {
       g_last_cuda_error = (int)e;
       return FA_ERR_NO_MEMORY;
     }
     p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_o);
-    p.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + bytes_o + bytes_ml);
-    e = cudaMemsetAsync(p.counters, 0, bytes_c, strm);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(ws, strm);
-      return cuda_fail(e);
-    }
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                         (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
   }
   cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)units, strm);
   if (ws) cudaFreeAsync(ws, strm);

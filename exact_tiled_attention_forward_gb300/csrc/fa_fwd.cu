@@ -11,23 +11,30 @@
 // from L2 after the first touch. Causal tiles that are fully masked are never
 // loaded ("What interviewers probe next").
 //
-// CTA layout (320 threads, one CTA per SM):
-//   warps 0-3  softmax + epilogue for query tile A (rows q0 .. q0+127)
-//   warps 4-7  softmax + epilogue for query tile B (rows q0+128 .. q0+255)
-//   warp  8    TMA producer (Q once, then K_j, V_j into a ring of stages)
-//   warp  9    TMEM allocator and tcgen05 MMA issuer
+// CTA layout (384 threads = three warpgroups, one CTA per SM):
+//   warpgroup 0 (warps 0-3)  softmax + epilogue for query tile A (rows q0 .. q0+127)
+//   warpgroup 1 (warps 4-7)  softmax + epilogue for query tile B (rows q0+128 .. q0+255)
+//   warpgroup 2: warp 8 TMA producer, warp 9 TMEM allocator + tcgen05 MMA
+//                issuer, warps 10-11 idle
+// One thread per query row (TMEM lane). Registers: launched at 168 per
+// thread; warpgroup 2 gives registers back (setmaxnreg 56) and the softmax
+// warpgroups take them (224 each): 128 x (224 + 224 + 56) = 64,512 =
+// 384 x 168, so the increase always fits.
+//
 // Tensor memory (512 columns x 128 lanes, FP32):
-//   [0,128) S_A / P_A   [128,256) S_B / P_B   [256,256+d) O_A   [384,384+d) O_B
-// P (BF16, two per column) overwrites the first 64 columns of its S tile and
-// is the A operand of the PV MMA straight from tensor memory.
+//   [0,128) S_A   [128,256) S_B   [256,256+d) O_A   [384,384+d) O_B
+// P (BF16, two per column) overwrites the first 64 columns of its S tile
+// (all 128 scores of a row are in registers first) and is the A operand of the
+// PV MMA straight from tensor memory.
 // MMA issue order per key tile j (ping-pong between the two query tiles):
 //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-// so the tensor core works on one tile while the other tile's softmax runs.
 // The commit that signals S_X(j+1) also covers PV_X(j): when a softmax warp
 // sees S_X(j+1) the accumulator O_X is stable and may be rescaled in place.
 //
-// Lazy rescale: a row keeps its reference max until a tile's max exceeds it by
-// more than 2^8 (log2 units); until then P <= 2^8, exact in the final O / l
+// Softmax per tile: exponentials are computed against the row's reference max
+// while the tile max is found alongside; only if a row's max rose by more
+// than 2^8 (log2 units) — always on its first live tile — is the tile redone
+// with the new reference and O, l rescaled. Until then P <= 2^8, exact in the final O / l
 // because O and l share the same stale reference.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -38,7 +45,11 @@ namespace fa {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 224;   // per thread, warpgroups 0-1
+constexpr int kRegsOther = 56;      // per thread, warpgroup 2
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -55,8 +66,8 @@ struct Cfg {
   static constexpr int kBarQ = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
-  static constexpr int kBarS = 1 + 2 * kStages;      // 2
-  static constexpr int kBarP = 3 + 2 * kStages;      // 2
+  static constexpr int kBarS = 1 + 2 * kStages;      // [2]
+  static constexpr int kBarP = 3 + 2 * kStages;      // [2]
   static constexpr int kBarO = 5 + 2 * kStages;
   static constexpr int kBarDrain = 6 + 2 * kStages;
   static constexpr int kNumBars = 7 + 2 * kStages;
@@ -70,6 +81,45 @@ struct Cfg {
 
 __device__ __forceinline__ int min_i(int a, int b) { return a < b ? a : b; }
 __device__ __forceinline__ int max_i(int a, int b) { return a > b ? a : b; }
+
+// P = 2^(s*c - mb) for the 128 scores of this thread's row (FP32 pairs, one
+// packed FMA per pair), packed to BF16 and stored over the first 64 columns
+// of the row's S tile in TMEM. Returns the row sum of P (FP32); if mx is not
+// null it also returns the max of the raw scores.
+__device__ __forceinline__ float exp_tile(const float* s, float c, float mb, uint32_t tS, float* mx) {
+  float2 sa = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    // the 32 exponentials of this chunk first (independent: the exp unit stays busy)
+    float pv[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 e = ffma2_bc(make_float2(s[cc * 32 + i], s[cc * 32 + i + 1]), c, -mb);
+      pv[i] = ex2_approx(e.x);
+      pv[i + 1] = ex2_approx(e.y);
+    }
+    // then BF16 packing and the TMEM store, row sums, running max of the raw scores
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
+    tmem_st16(tS + cc * 16, pk);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      sa = fadd2(sa, make_float2(pv[i], pv[i + 1]));
+      sb2 = fadd2(sb2, make_float2(pv[i + 2], pv[i + 3]));
+    }
+    if (mx) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        m0 = max3f(m0, s[cc * 32 + i], s[cc * 32 + i + 1]);
+        m1 = max3f(m1, s[cc * 32 + i + 2], s[cc * 32 + i + 3]);
+      }
+    }
+  }
+  if (mx) *mx = fmaxf(m0, m1);
+  return (sa.x + sa.y) + (sb2.x + sb2.y);
+}
 
 // Bounded wait used on drain paths: ignores the abort flag, still gives up after the timeout.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
@@ -89,18 +139,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: (b, h, query block, key-range split), head-major, longest first
-  const int S = p.splits;
+  // ---- work unit. Units [0, u_full) are whole query blocks written directly;
+  // the rest split the last query blocks' key ranges into s_tail parts whose
+  // partial (m, l, O) go to the workspace (merged by fa_merge_kernel). Query
+  // blocks are numbered head-major (a head's blocks are adjacent, so its K/V
+  // stay in L2); causal blocks run longest first within a head.
   const int u = blockIdx.x;
-  const int split = u % S;
-  const int t_ = u / S;
-  const int qr = t_ % p.n_qb;
-  const int bh = t_ / p.n_qb;
+  int qlin, split, S, slot;
+  if (u < p.u_full) {
+    qlin = u; split = 0; S = 1; slot = -1;
+  } else {
+    const int v = u - p.u_full;
+    qlin = p.u_full + v / p.s_tail; split = v % p.s_tail; S = p.s_tail; slot = v;
+  }
+  const int qr = qlin % p.n_qb;
+  const int bh = qlin / p.n_qb;
   const int qb = p.causal ? (p.n_qb - 1 - qr) : qr;
   const int b = bh / p.H_q;
   const int h = bh - b * p.H_q;
@@ -108,26 +165,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qb * kBlockRows;
 
   // key tiles each query tile needs: [0, kv_hi[X]); fully masked tiles are never visited
-  int kv_hi[2];
+  int kv_hi0, kv_hi1;
+  {
+    int kvh[2];
 #pragma unroll
-  for (int X = 0; X < 2; ++X) {
-    const int first = q0 + X * kTileM;
-    if (first >= p.N_q) {
-      kv_hi[X] = 0;
-    } else if (!p.causal) {
-      kv_hi[X] = p.n_kv_tiles;
-    } else {
-      const int last_key = min_i(first + kTileM - 1, p.N_q - 1) + p.kv_off;
-      kv_hi[X] = last_key < 0 ? 0 : min_i(p.n_kv_tiles, last_key / kTileN + 1);
+    for (int X = 0; X < 2; ++X) {
+      const int first = q0 + X * kTileM;
+      if (first >= p.N_q) {
+        kvh[X] = 0;
+      } else if (!p.causal) {
+        kvh[X] = p.n_kv_tiles;
+      } else {
+        const int last_key = min_i(first + kTileM - 1, p.N_q - 1) + p.kv_off;
+        kvh[X] = last_key < 0 ? 0 : min_i(p.n_kv_tiles, last_key / kTileN + 1);
+      }
     }
+    kv_hi0 = kvh[0];
+    kv_hi1 = kvh[1];
   }
-  const int n_all = max_i(kv_hi[0], kv_hi[1]);
+  const int n_all = max_i(kv_hi0, kv_hi1);
   const int lo = (int)(((long long)split * n_all) / S);
   const int hi = (int)(((long long)(split + 1) * n_all) / S);
-  int nX[2];
-  nX[0] = max_i(0, min_i(hi, kv_hi[0]) - lo);
-  nX[1] = max_i(0, min_i(hi, kv_hi[1]) - lo);
-  const int nmax = max_i(nX[0], nX[1]);
+  const int n0 = max_i(0, min_i(hi, kv_hi0) - lo);
+  const int n1 = max_i(0, min_i(hi, kv_hi1) - lo);
+  const int nmax = max_i(n0, n1);
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -138,19 +199,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::kBarS + 0), 1);
     mbar_init(bar(C::kBarS + 1), 1);
-    mbar_init(bar(C::kBarP + 0), 128);
+    mbar_init(bar(C::kBarP + 0), 128);   // all 128 rows of the tile
     mbar_init(bar(C::kBarP + 1), 128);
     mbar_init(bar(C::kBarO), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *s_abort = 0;
-    *s_last = 0;
     fence_mbar_init();
+    // the merge kernel (launched as a programmatic dependent) may be scheduled
+    // once every CTA of this grid has started; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kWarpProducer && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -160,124 +223,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ======================= TMA producer =======================
-    if (lane == 0 && nmax > 0) {
-      int issued = 0;  // K/V tile loads issued
-      mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+    if (warp == kWarpProducer) {
+      // ======================= TMA producer =======================
+      if (lane == 0 && nmax > 0) {
+        int issued = 0;  // K/V tile loads issued
+        mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
 #pragma unroll
-      for (int X = 0; X < 2; ++X)
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_3d(sb + C::kOffQ + X * C::kTileBytes + bx * C::kBoxBytes, &tmQ, bar(C::kBarQ),
-                      bx * 64, q0 + X * kTileM, bh);
-      const uint64_t pol = policy_evict_last();
-      bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int tile = lo + j;
-#pragma unroll
-        for (int sel = 0; sel < 2; ++sel) {  // 0: K tile, 1: V tile
-          const int it = 2 * j + sel;
-          const int st = it % C::kStages;
-          const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-          if (!mbar_wait(bar(C::kBarEmpty + st), ph ^ 1u, s_abort, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(C::kBarFull + st), C::kTileBytes);
+        for (int X = 0; X < 2; ++X)
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d_hint(sb + C::kOffKV + st * C::kTileBytes + bx * C::kBoxBytes,
-                             sel ? (const void*)&tmV : (const void*)&tmK, bar(C::kBarFull + st),
-                             bx * 64, tile * kTileN, bhk, pol);
-          ++issued;
-        }
-      }
-      // drain: every load issued has landed before the CTA may exit
-      drain_wait(bar(C::kBarQ), 0, p.status);
-      for (int st = 0; st < C::kStages; ++st) {
-        const int n_st = issued > st ? (issued - st + C::kStages - 1) / C::kStages : 0;
-        if (n_st > 0) drain_wait(bar(C::kBarFull + st), (uint32_t)(n_st - 1) & 1u, p.status);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ======================= tcgen05 MMA issuer =======================
-    if (lane == 0 && nmax > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, kTileN, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
-      auto issue_S = [&](int X, int st) {
-        const uint32_t qa = sb + C::kOffQ + X * C::kTileBytes;
-        const uint32_t kb = sb + C::kOffKV + st * C::kTileBytes;
+            tma_load_3d(sb + C::kOffQ + X * C::kTileBytes + bx * C::kBoxBytes, &tmQ, bar(C::kBarQ),
+                        bx * 64, q0 + X * kTileM, bh);
+        const uint64_t pol = policy_evict_last();
+        bool ok = true;
+        for (int j = 0; j < nmax && ok; ++j) {
+          const int tile = lo + j;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::tm_s(X), smem_desc_sw128(qa + off, 16, 1024),
-                 smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_PV = [&](int X, int st, bool acc) {
-        const uint32_t vb = sb + C::kOffKV + st * C::kTileBytes;
+          for (int sel = 0; sel < 2; ++sel) {  // 0: K tile, 1: V tile
+            const int it = 2 * j + sel;
+            const int st = it % C::kStages;
+            const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+            if (!mbar_wait(bar(C::kBarEmpty + st), ph ^ 1u, s_abort, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(C::kBarFull + st), C::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          mma_ts(tmem + C::tm_o(X), tmem + C::tm_s(X) + kk * 8,
-                 smem_desc_sw128(vb + kk * 16 * 128, C::kBoxBytes, 1024), idO,
-                 (acc || kk > 0) ? 1u : 0u);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_3d_hint(sb + C::kOffKV + st * C::kTileBytes + bx * C::kBoxBytes,
+                               sel ? (const void*)&tmV : (const void*)&tmK, bar(C::kBarFull + st),
+                               bx * 64, tile * kTileN, bhk, pol);
+            ++issued;
+          }
         }
-      };
-      bool ok = mbar_wait(bar(C::kBarQ), 0, s_abort, p.status);
-      if (ok) ok = mbar_wait(bar(C::kBarFull + 0), 0, s_abort, p.status);
-      if (ok) {
-        tc_fence_after();
-        if (nX[0] > 0) { issue_S(0, 0); mma_commit(bar(C::kBarS + 0)); }
-        if (nX[1] > 0) { issue_S(1, 0); mma_commit(bar(C::kBarS + 1)); }
-        mma_commit(bar(C::kBarEmpty + 0));
-      }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int itV = 2 * j + 1, itK = 2 * j + 2;
-        const int stV = itV % C::kStages, stK = itK % C::kStages;
-        const uint32_t phV = (uint32_t)(itV / C::kStages) & 1u;
-        const uint32_t phK = (uint32_t)(itK / C::kStages) & 1u;
-        const bool next = (j + 1) < nmax;
-        if (!(ok = mbar_wait(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
-        tc_fence_after();
-        if (j < nX[0]) {
-          if (!(ok = mbar_wait(bar(C::kBarP + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
-          tc_fence_after();
-          issue_PV(0, stV, j > 0);
-        }
-        if (next) {
-          if (!(ok = mbar_wait(bar(C::kBarFull + stK), phK, s_abort, p.status))) break;
-          tc_fence_after();
-          if (j + 1 < nX[0]) { issue_S(0, stK); mma_commit(bar(C::kBarS + 0)); }
-        }
-        if (j < nX[1]) {
-          if (!(ok = mbar_wait(bar(C::kBarP + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
-          tc_fence_after();
-          issue_PV(1, stV, j > 0);
-        }
-        mma_commit(bar(C::kBarEmpty + stV));
-        if (next) {
-          if (j + 1 < nX[1]) { issue_S(1, stK); mma_commit(bar(C::kBarS + 1)); }
-          mma_commit(bar(C::kBarEmpty + stK));
+        // drain: every load issued has landed before the CTA may exit
+        drain_wait(bar(C::kBarQ), 0, p.status);
+        for (int st = 0; st < C::kStages; ++st) {
+          const int n_st = issued > st ? (issued - st + C::kStages - 1) / C::kStages : 0;
+          if (n_st > 0) drain_wait(bar(C::kBarFull + st), (uint32_t)(n_st - 1) & 1u, p.status);
         }
       }
-      mma_commit(bar(C::kBarO));
-      // drain: all MMAs done before tensor memory is released
-      mma_commit(bar(C::kBarDrain));
-      drain_wait(bar(C::kBarDrain), 0, p.status);
+      __syncwarp();
+    } else if (warp == kWarpMma) {
+      // ======================= tcgen05 MMA issuer =======================
+      if (lane == 0 && nmax > 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, kTileN, false);
+        constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+        // Descriptors are built once; each MMA adds a compile-time offset to the
+        // start-address field (16-byte units) of the low word, so issuing stays
+        // ahead of the tensor core.
+        constexpr uint32_t kStageStep = (uint32_t)(C::kTileBytes >> 4);
+        constexpr uint32_t kHi = desc_sw128_hi(1024);
+        const uint32_t lq0 = desc_sw128_lo(sb + C::kOffQ, 16);
+        const uint32_t lk0 = desc_sw128_lo(sb + C::kOffKV, 16);
+        const uint32_t lv0 = desc_sw128_lo(sb + C::kOffKV, C::kBoxBytes);
+        auto issue_S = [&](int X, int st) {
+          const uint32_t a0 = lq0 + (uint32_t)X * kStageStep;
+          const uint32_t b0 = lk0 + (uint32_t)st * kStageStep;
+          const uint32_t d = tmem + C::tm_s(X);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
+            const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+            mma_ss_lh(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_PV = [&](int X, int st, bool acc) {
+          const uint32_t b0 = lv0 + (uint32_t)st * kStageStep;
+          const uint32_t d = tmem + C::tm_o(X);
+          const uint32_t a = tmem + C::tm_s(X);
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 16kk .. 16kk+15 in columns 8kk ..
+            mma_ts_lh(d, a + (uint32_t)kk * 8u,
+                      b0 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO, (acc || kk > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait(bar(C::kBarQ), 0, s_abort, p.status);
+        if (ok) ok = mbar_wait(bar(C::kBarFull + 0), 0, s_abort, p.status);
+        if (ok) {
+          tc_fence_after();
+          if (n0 > 0) { issue_S(0, 0); mma_commit(bar(C::kBarS + 0)); }
+          if (n1 > 0) { issue_S(1, 0); mma_commit(bar(C::kBarS + 1)); }
+          mma_commit(bar(C::kBarEmpty + 0));
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+          const int itV = 2 * j + 1, itK = 2 * j + 2;
+          const int stV = itV % C::kStages, stK = itK % C::kStages;
+          const uint32_t phV = (uint32_t)(itV / C::kStages) & 1u;
+          const uint32_t phK = (uint32_t)(itK / C::kStages) & 1u;
+          const bool next = (j + 1) < nmax;
+          if (!(ok = mbar_wait(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
+          tc_fence_after();
+          if (j < n0) {
+            if (!(ok = mbar_wait(bar(C::kBarP + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
+            tc_fence_after();
+            issue_PV(0, stV, j > 0);
+          }
+          if (next) {
+            if (!(ok = mbar_wait(bar(C::kBarFull + stK), phK, s_abort, p.status))) break;
+            tc_fence_after();
+            if (j + 1 < n0) { issue_S(0, stK); mma_commit(bar(C::kBarS + 0)); }
+          }
+          if (j < n1) {
+            if (!(ok = mbar_wait(bar(C::kBarP + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
+            tc_fence_after();
+            issue_PV(1, stV, j > 0);
+          }
+          mma_commit(bar(C::kBarEmpty + stV));
+          if (next) {
+            if (j + 1 < n1) { issue_S(1, stK); mma_commit(bar(C::kBarS + 1)); }
+            mma_commit(bar(C::kBarEmpty + stK));
+          }
+        }
+        mma_commit(bar(C::kBarO));
+        // drain: all MMAs done before tensor memory is released
+        mma_commit(bar(C::kBarDrain));
+        drain_wait(bar(C::kBarDrain), 0, p.status);
+      }
+      __syncwarp();
     }
-    __syncwarp();
+    // warps 10-11: idle members of warpgroup 2
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ======================= softmax warpgroups =======================
-    const int X = warp >> 2;
+    const int X = warp >> 2;                // query tile
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;           // row within the query tile = TMEM lane
-    const int row = q0 + X * kTileM + r;      // query row within the head
+    const int r = quad * 32 + lane;         // row within the query tile = TMEM lane
+    const int row = q0 + X * kTileM + r;    // query row within the head
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::tm_s(X);
     const uint32_t tO = tmem + lane_base + C::tm_o(X);
-    const int n = nX[X];
+    const int n = X ? n1 : n0;
     const float c = p.c;
     const int tile_first_row = q0 + X * kTileM;
     float m_ref = -INFINITY;  // reference max, scaled log2 units
@@ -302,60 +379,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kTileN; ++i)
           if (i >= lim) s[i] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // warp-uniform: every row of the warp has a reference max
+      const bool spec = !__any_sync(0xffffffffu, m_ref == -INFINITY);
+      float rs = 0.f, mx;
+      if (spec) {
+        rs = exp_tile(s, c, m_ref, tS, &mx);
+      } else {
+        float a0 = s[0], a1 = s[1];
 #pragma unroll
-      for (int i = 4; i < kTileN; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
+        for (int i = 2; i < kTileN - 2; i += 4) {
+          a0 = max3f(a0, s[i], s[i + 1]);
+          a1 = max3f(a1, s[i + 2], s[i + 3]);
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(s[kTileN - 2], s[kTileN - 1]));
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      const bool need = m_tile > m_ref + kTau;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_ref - m_tile);  // 0 on the first live tile
-        m_ref = m_tile;
-        l *= alpha;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_X holds PV_X(0..j-1) and is stable (covered by the S_X(j) commit)
+      const float m_tile = mx * c;
+      const bool need = m_tile > m_ref + kTau;   // always true on a row's first live tile
+      const bool any_need = __any_sync(0xffffffffu, need);
+      if (any_need) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_ref - m_tile);  // 0 when the row had no reference yet
+          m_ref = m_tile;
+          l *= alpha;
+        }
+        if (j > 0) {
+          // O_X holds PV_X(0..j-1) and is stable (covered by the S_X(j) commit)
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          float ov[32];
-          tmem_ld32(tO + cc, ov);
-          tmem_wait_ld();
+          for (int cc = 0; cc < D; cc += 32) {
+            float ov[32];
+            tmem_ld32(tO + cc, ov);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-          tmem_st32(tO + cc, ov);
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            tmem_st32(tO + cc, ov);
+          }
         }
       }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[cc * 32 + 2 * i], c, -mb));
-          const float p1 = ex2_approx(fmaf(s[cc * 32 + 2 * i + 1], c, -mb));
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + cc * 16, pk);
-      }
-      l += rs0 + rs1;
+      if (any_need || !spec) rs = exp_tile(s, c, m_ref == -INFINITY ? 0.f : m_ref, tS, nullptr);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarP + X));
+      l += rs;
     }
     if (ok && n > 0) {
       ok = mbar_wait(bar(C::kBarO), 0, s_abort, p.status);
       tc_fence_after();
     }
     const bool valid_row = row < p.N_q;
-    if (S == 1) {
+    if (slot < 0) {
       // ---- final epilogue: O / l -> BF16, LSE
       if (ok) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -383,86 +455,129 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid_row && p.lse)
           p.lse[(size_t)bh * p.N_q + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
-    } else {
-      // ---- partial: unnormalised O, (m, l) to the workspace; last CTA of the block merges
-      const size_t blk = (size_t)bh * p.n_qb + qb;
-      const size_t prow = (blk * S + split) * kBlockRows + X * kTileM + r;
-      if (ok) {
-        float* po = p.part_o + prow * D;
+    } else if (ok) {
+      // ---- partial: unnormalised O and (m, l) of this key range to the workspace
+      const size_t prow = (size_t)slot * kBlockRows + X * kTileM + r;
+      float* po = p.part_o + prow * D;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          float ov[32];
-          if (n > 0) {
-            tmem_ld32(tO + cc, ov);
-            tmem_wait_ld();
-          } else {
+      for (int cc = 0; cc < D; cc += 32) {
+        float ov[32];
+        if (n > 0) {
+          tmem_ld32(tO + cc, ov);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-          }
+          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            __stcg(reinterpret_cast<float4*>(po + cc) + g,
-                   make_float4(ov[4 * g], ov[4 * g + 1], ov[4 * g + 2], ov[4 * g + 3]));
-        }
-        __stcg(reinterpret_cast<float2*>(p.part_ml) + prow, make_float2(l > 0.f ? m_ref : -INFINITY, l));
-        __threadfence();
+        for (int g = 0; g < 8; ++g)
+          __stcg(reinterpret_cast<float4*>(po + cc) + g,
+                 make_float4(ov[4 * g], ov[4 * g + 1], ov[4 * g + 2], ov[4 * g + 3]));
       }
-      named_bar_sync(1, 256);
-      if (threadIdx.x == 0) {
-        int last = 0;
-        if (!*s_abort) last = (atomicAdd(p.counters + blk, 1) == S - 1);
-        *s_last = last;
-      }
-      named_bar_sync(1, 256);
-      if (*s_last && ok) {
-        __threadfence();
-        const size_t rbase = blk * S * kBlockRows + X * kTileM + r;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < S; ++s2) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + rbase + (size_t)s2 * kBlockRows);
-          if (ml.y > 0.f) M = fmaxf(M, ml.x);
-        }
-        float L = 0.f;
-        for (int s2 = 0; s2 < S; ++s2) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + rbase + (size_t)s2 * kBlockRows);
-          if (ml.y > 0.f) L += ex2_approx(ml.x - M) * ml.y;
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        if (valid_row) {
-          __nv_bfloat16* orow =
-              reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N_q + row) * D;
-#pragma unroll 1
-          for (int cc = 0; cc < D; cc += 8) {
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            for (int s2 = 0; s2 < S; ++s2) {
-              const size_t pr = rbase + (size_t)s2 * kBlockRows;
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pr);
-              if (!(ml.y > 0.f)) continue;
-              const float w = ex2_approx(ml.x - M) * inv;
-              const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + cc));
-              const float4 b2 = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + cc) + 1);
-              acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-              acc[4] += w * b2.x; acc[5] += w * b2.y; acc[6] += w * b2.z; acc[7] += w * b2.w;
-            }
-            st_global_v4(orow + cc, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-          }
-          if (p.lse)
-            p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
-        }
-      }
+      __stcg(reinterpret_cast<float2*>(p.part_ml) + prow,
+             make_float2(l > 0.f ? m_ref : -INFINITY, l));
     }
   }
 
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+// Merge of the split-key partials (the online-softmax merge of page 2, "The
+// Tiling Algorithm", applied to whole key ranges): for each query row of a
+// split block, M = max_s m_s, L = sum_s 2^(m_s - M) l_s, O = sum_s 2^(m_s - M)
+// O_s / L, LSE = (M + log2 L) ln 2. One warp per row, lanes across columns.
+// Launched as a programmatic dependent of fa_fwd_kernel: it may be resident
+// early and waits (griddepcontrol.wait) until that grid has completed.
+template <int D>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kCols = D / 32;  // columns per lane
+  const int lane = threadIdx.x & 31;
+  const long long wrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int t = (int)(wrow / kBlockRows);
+  const int r = (int)(wrow % kBlockRows);
+  if (t >= p.n_tail) return;
+  const int qlin = p.u_full + t;
+  const int bh = qlin / p.n_qb;
+  const int qr = qlin % p.n_qb;
+  const int qb = p.causal ? (p.n_qb - 1 - qr) : qr;
+  const int row = qb * kBlockRows + r;
+  if (row >= p.N_q) return;
+  const int S = p.s_tail;
+  const size_t base = (size_t)t * S * kBlockRows + r;  // partial row of split 0
+  float m = -INFINITY, l = 0.f;
+  if (lane < S) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + (size_t)lane * kBlockRows);
+    if (ml.y > 0.f) {
+      m = ml.x;
+      l = ml.y;
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = (l > 0.f) ? ex2_approx(m - M) : 0.f;
+  float L = w * l;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float acc[kCols];
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int s2 = 0; s2 < S; ++s2) {
+    const float ws = __shfl_sync(0xffffffffu, w, s2) * inv;
+    const float* src = p.part_o + (base + (size_t)s2 * kBlockRows) * D + lane * kCols;
+    if constexpr (kCols == 4) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+      acc[0] += ws * a.x; acc[1] += ws * a.y; acc[2] += ws * a.z; acc[3] += ws * a.w;
+    } else {
+      const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
+      acc[0] += ws * a.x; acc[1] += ws * a.y;
+    }
+  }
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N_q + row) * D;
+  if constexpr (kCols == 4) {
+    uint2 v;
+    v.x = pack_bf16x2(acc[0], acc[1]);
+    v.y = pack_bf16x2(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(orow + lane * 4) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack_bf16x2(acc[0], acc[1]);
+  }
+  if (lane == 0 && p.lse) p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, int units, cudaStream_t stream) {
+  static bool attr = false;  // benign race: setting the attribute twice is harmless
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  fa_fwd_kernel<D><<<units, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_tail == 0) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(((long long)p.n_tail * kBlockRows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_merge_kernel<D>, p);
 }
 
 }  // namespace
@@ -474,26 +589,8 @@ size_t fwd_smem_bytes(int d) {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int units, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  if (d == 128) {
-    static bool attr = false;  // benign race: setting the attribute twice is harmless
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Cfg<128>::kSmemBytes);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    fa_fwd_kernel<128><<<units, kThreads, Cfg<128>::kSmemBytes, stream>>>(tq, tk, tv, p);
-  } else {
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Cfg<64>::kSmemBytes);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    fa_fwd_kernel<64><<<units, kThreads, Cfg<64>::kSmemBytes, stream>>>(tq, tk, tv, p);
-  }
-  return cudaGetLastError();
+  return d == 128 ? launch_fwd_t<128>(tq, tk, tv, p, units, stream)
+                  : launch_fwd_t<64>(tq, tk, tv, p, units, stream);
 }
 
 }  // namespace fa

@@ -19,20 +19,30 @@ struct FwdParams {
   int kv_off;       // N_k - N_q: query i sees key j iff j <= i + kv_off (causal)
   int n_qb;         // query blocks of kBlockRows rows per (b, h)
   int n_kv_tiles;   // ceil(N_k / kTileN)
-  int splits;       // key-range splits per query block (1 = no merge)
+  int u_full;       // units [0, u_full) are whole query blocks (query blocks 0 .. u_full-1)
+  int n_tail;       // query blocks u_full .. u_full+n_tail-1 are split ...
+  int s_tail;       // ... into s_tail key ranges each (units u_full + t*s_tail + s)
   float c;          // scale * log2(e)
   void* o;          // bf16 [B][H_q][N_q][d]
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
-  float* part_o;    // fp32 [units][kBlockRows][d]        (splits > 1)
-  float* part_ml;   // fp32 [units][kBlockRows][2] (m, l)  (splits > 1)
-  int* counters;    // int  [B*H_q*n_qb], zeroed           (splits > 1)
+  float* part_o;    // fp32 [n_tail*s_tail][kBlockRows][d]        (n_tail > 0)
+  float* part_ml;   // fp32 [n_tail*s_tail][kBlockRows][2] (m, l)  (n_tail > 0)
   int* status;      // device status word
 };
+
+// How the query blocks of one call are cut into CTAs (see FwdParams).
+struct FwdPlan {
+  int u_full, n_tail, s_tail;
+  long long units;      // CTAs of the fused kernel
+  size_t part_bytes;    // workspace for the split partials (0 when n_tail == 0)
+};
+FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms);
 
 // Shared-memory bytes the fused kernel needs for head dim d (64 or 128).
 size_t fwd_smem_bytes(int d);
 
-// Launch the fused kernel over `units` = B*H_q*n_qb*splits CTAs.
+// Launch the fused kernel over `units` CTAs, then (if p.n_tail > 0) the merge
+// kernel as its programmatic dependent on the same stream.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int units, cudaStream_t stream);
 
@@ -71,8 +81,6 @@ int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st);
 // Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 int num_sms();
-// Key-range splits per query block for `blocks` blocks of `kv_tiles` key tiles.
-int choose_splits(long long blocks, int kv_tiles, int sms);
 extern thread_local int g_last_cuda_error;
 
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.

@@ -18,10 +18,11 @@ namespace fa {
 namespace {
 
 // Scratch for the split-key partials: per split CTA, kBlockRows rows of FP32
-// O (d values) plus (m, l), followed by one int counter per query block.
-// 32 MiB: enough for every split the planner picks at d = 128 up to about
-// 250 split CTAs (the 1-head N = 8192 workload needs 17 MiB). Every GPU that
-// loads libfa holds this array until the process exits.
+// O (d values) plus (m, l). 32 MiB holds up to 252 split CTAs at d = 128
+// (the 1-head N = 8192 workload uses 128 of them, 17 MiB). Every GPU that
+// loads libfa holds this array until the process exits. Nothing in it needs
+// to start at zero: every partial row the merge reads is written first by
+// the same call.
 constexpr size_t kScratchBytes = 32u << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -78,23 +79,20 @@ extern "C" int fa_forward_noalloc(const void* q, const void* k, const void* v, v
   p.status = status;
   const long long blocks = (long long)B * H_q * p.n_qb;
   const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
-  p.splits = choose_splits(blocks, kv_eff, num_sms());
-  const long long units = blocks * p.splits;
-  if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
+  if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  p.u_full = pl.u_full;
+  p.n_tail = pl.n_tail;
+  p.s_tail = pl.s_tail;
+  const long long units = pl.units;
 
-  if (p.splits > 1) {
-    const size_t n_rows = (size_t)units * kBlockRows;
-    const size_t bytes_o = n_rows * d * 4, bytes_ml = n_rows * 8, bytes_c = (size_t)blocks * 4;
-    if (bytes_o + bytes_ml + bytes_c > kScratchBytes) return FA_ERR_TOO_LARGE;
+  if (pl.n_tail > 0) {
+    if (pl.part_bytes > kScratchBytes) return FA_ERR_TOO_LARGE;
     int err = 0;
     char* base = static_cast<char*>(scratch_address(&err));
     if (!base) return cuda_fail((cudaError_t)err);
     p.part_o = reinterpret_cast<float*>(base);
-    p.part_ml = reinterpret_cast<float*>(base + bytes_o);
-    p.counters = reinterpret_cast<int*>(base + bytes_o + bytes_ml);
-    // the merge counters must start at zero; the array keeps the previous call's values
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, bytes_c, strm);
-    if (e != cudaSuccess) return cuda_fail(e);
+    p.part_ml = reinterpret_cast<float*>(base + (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
   }
 
   CUtensorMap tq, tk, tv;

@@ -58,10 +58,10 @@ typedef enum {
 
 /* Exact attention forward, fused (the tiled online-softmax kernel).
  * Prefill (N_q > 1 or B*H_q large): tcgen05/TMA kernel, two 128-row query
- * tiles per CTA, K/V tiles of 128 keys. When there are too few query blocks to
- * fill the GPU, the key range of each block is split over several CTAs and the
- * partial (m, l, O) results are merged in-kernel. Decode (N_q == 1): split-K
- * kernel over 256-key chunks with GQA, followed by the same merge.
+ * tiles per CTA, K/V tiles of 128 keys. Query blocks that do not fill a whole
+ * wave of the GPU have their key range split over several CTAs; a second
+ * kernel (programmatic dependent launch on the same stream) merges the
+ * partial (m, l, O) results.
  * Split and decode partials live in a stream-ordered workspace taken from a
  * library-owned memory pool on the current device (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`); the pool keeps freed memory reserved for later
@@ -87,8 +87,8 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
  * Sharing: every call uses the same array, which keeps the last call's
- * contents (the merge counters are cleared with cudaMemsetAsync on `stream`
- * at each call). Calls whose execution overlaps on the GPU race on the array:
+ * contents (each call writes every partial it reads, so nothing needs
+ * clearing). Calls whose execution overlaps on the GPU race on the array:
  * issue them on one stream, or order them with events. */
 int fa_forward_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,

@@ -7,6 +7,11 @@ import oracle
 TOL_MAX_ABS_O = 1e-2
 TOL_REL_L2_O = 5e-3
 TOL_MAX_ABS_LSE = 1e-3
+# Element-wise, the absolute bound on O is widened for large |O|: the BF16
+# output alone rounds a value by up to 2^-8 |O| (half an ulp), which exceeds
+# 1e-2 once |O| >= 2.56, and BF16 probabilities add up to 2^-9 |O|. So each
+# element must satisfy |dO| <= max(1e-2, 6e-3 |O_ref|) (6e-3 > 2^-8 + 2^-9).
+TOL_REL_ELEM_O = 6e-3
 
 
 def to_dev(bits):
@@ -28,9 +33,11 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL
     assert np.isfinite(o_gpu).all(), "non-finite values in O"
     err = np.abs(o_gpu - o_ref)
     max_abs = float(err.max()) if err.size else 0.0
+    bound = np.maximum(tol_o, TOL_REL_ELEM_O * np.abs(o_ref))
+    worst = float((err / bound).max()) if err.size else 0.0
     denom = float(np.linalg.norm(o_ref))
     rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))
-    res = {"max_abs_o": max_abs, "rel_l2_o": rel}
+    res = {"max_abs_o": max_abs, "rel_l2_o": rel, "worst_over_bound": worst}
     if lse_ref is not None:
         lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
         inf_ref = np.isneginf(lse_ref)
@@ -39,7 +46,7 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL
         lerr = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
         res["max_abs_lse"] = lerr
         assert lerr <= tol_lse, res
-    assert max_abs <= tol_o, res
+    assert worst <= 1.0, res
     assert rel <= tol_rel, res
     return res
 

@@ -15,7 +15,7 @@ import pytest
 
 from exact_tiled_attention_forward_gb300 import inputs as I
 
-from helpers import TOL_MAX_ABS_O, TOL_REL_L2_O, TOL_MAX_ABS_LSE, to_dev
+from helpers import TOL_MAX_ABS_O, TOL_REL_ELEM_O, TOL_REL_L2_O, TOL_MAX_ABS_LSE, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -46,22 +46,25 @@ def _call(fa, entry, q, k, v, o, lse, a):
 
 
 def _planned_scratch(a, sms):
-    """Scratch bytes the planner's split needs (mirrors choose_splits in libfa)."""
+    """Scratch bytes of the split partials the planner picks (mirrors plan_forward in libfa)."""
     n_qb = (a.N_q + 255) // 256
     n_kv = (a.N_k + 127) // 128
     kv_eff = (n_kv + 1) // 2 if a.causal else n_kv
     blocks = a.B * a.H_q * n_qb
+    if blocks <= 0 or kv_eff <= 1:
+        return 0
+    tail = blocks if blocks < sms else (0 if a.causal else blocks % sms)
+    if tail == 0:
+        return 0
     best, best_cost = 1, 1e30
-    if not (kv_eff <= 1 or blocks >= 2 * sms):
-        for s in range(1, min(16, kv_eff) + 1):
-            waves = (blocks * s + sms - 1) // sms
-            cost = waves * (2.0 + kv_eff / s)
-            if cost < best_cost - 1e-9:
-                best, best_cost = s, cost
+    for s in range(1, min(16, kv_eff) + 1):
+        waves = (tail * s + sms - 1) // sms
+        cost = waves * (2.0 + kv_eff / s) + (0.5 if s > 1 else 0.0)
+        if cost < best_cost - 1e-9:
+            best, best_cost = s, cost
     if best == 1:
         return 0
-    units = blocks * best
-    return units * 256 * (a.d * 4 + 8) + blocks * 4
+    return tail * best * 256 * (a.d * 4 + 8)
 
 
 @pytest.mark.parametrize("shape", [
@@ -89,7 +92,7 @@ def test_noalloc_matches_fa_forward_twice(fa, shape):
         got_l = l.cpu().numpy()
         assert np.isfinite(got_o).all()
         err = np.abs(got_o - ref_o)
-        assert err.max() <= TOL_MAX_ABS_O
+        assert (err <= np.maximum(TOL_MAX_ABS_O, TOL_REL_ELEM_O * np.abs(ref_o))).all()
         assert np.linalg.norm(got_o - ref_o) <= TOL_REL_L2_O * np.linalg.norm(ref_o)
         fin = np.isfinite(ref_l)
         assert np.array_equal(np.isfinite(got_l), fin)
