@@ -7,11 +7,19 @@ import oracle
 TOL_MAX_ABS_O = 1e-2
 TOL_REL_L2_O = 5e-3
 TOL_MAX_ABS_LSE = 1e-3
-# Element-wise, the absolute bound on O is widened for large |O|: the BF16
-# output alone rounds a value by up to 2^-8 |O| (half an ulp), which exceeds
-# 1e-2 once |O| >= 2.56, and BF16 probabilities add up to 2^-9 |O|. So each
-# element must satisfy |dO| <= max(1e-2, 6e-3 |O_ref|) (6e-3 > 2^-8 + 2^-9).
-TOL_REL_ELEM_O = 6e-3
+# Element-wise, the absolute bound on O is widened where the BF16 arithmetic
+# the method fixes cannot meet 1e-2: BF16 has unit roundoff u = 2^-8, so
+#   * rounding O itself to BF16 moves it by up to u |O|, and
+#   * each probability is rounded to BF16 before the PV product, which moves
+#     O_t = sum_j p_j v_jt / l by up to u * A_t with A_t = sum_j p_j |v_jt| / l.
+# A is the oracle's own definition evaluated on |V|. Each element must satisfy
+#   |dO| <= max(1e-2, TOL_REL_ELEM_O * (A + |O_ref|))   (5e-3 = 1.28 u).
+TOL_REL_ELEM_O = 5e-3
+
+
+def abs_values(v_bits):
+    """|V| as BF16 bit patterns (sign bit cleared; exact)."""
+    return np.asarray(v_bits, dtype=np.uint16) & np.uint16(0x7FFF)
 
 
 def to_dev(bits):
@@ -24,8 +32,8 @@ def bf16_dev_to_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL_L2_O,
-            tol_lse=TOL_MAX_ABS_LSE):
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
+            tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE):
     """Element-wise comparison of O and LSE; returns a dict of error figures."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
@@ -33,7 +41,8 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL
     assert np.isfinite(o_gpu).all(), "non-finite values in O"
     err = np.abs(o_gpu - o_ref)
     max_abs = float(err.max()) if err.size else 0.0
-    bound = np.maximum(tol_o, TOL_REL_ELEM_O * np.abs(o_ref))
+    a_ref = np.abs(o_ref) if o_abs_ref is None else np.asarray(o_abs_ref, dtype=np.float64)
+    bound = np.maximum(tol_o, TOL_REL_ELEM_O * (a_ref + np.abs(o_ref)))
     worst = float((err / bound).max()) if err.size else 0.0
     denom = float(np.linalg.norm(o_ref))
     rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))
@@ -52,4 +61,7 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, tol_o=TOL_MAX_ABS_O, tol_rel=TOL_REL
 
 
 def run_oracle(a):
-    return oracle.attention_reference(a.q, a.k, a.v, causal=a.causal, scale=a.scale)
+    """(O, LSE, A): the oracle's O and LSE, and A = the same attention of |V|."""
+    o, lse = oracle.attention_reference(a.q, a.k, a.v, causal=a.causal, scale=a.scale)
+    o_abs, _ = oracle.attention_reference(a.q, a.k, abs_values(a.v), causal=a.causal, scale=a.scale)
+    return o, lse, o_abs

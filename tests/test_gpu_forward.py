@@ -61,8 +61,7 @@ def test_small_shapes(fa, shape):
     B, Hq, Hkv, Nq, Nk, d, causal = shape
     a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=1)
     o, lse = _run(fa, a)
-    o_ref, lse_ref = run_oracle(a)
-    compare(o, lse, o_ref, lse_ref)
+    compare(o, lse, *run_oracle(a))
 
 
 def test_tiny_workload_n256_d64(fa):
@@ -129,8 +128,8 @@ def test_naive_matches_oracle(fa):
                   (2, 4, 2, 129, 129, 128, False)]:
         a = I.make_inputs(*shape[:6], causal=shape[6], seed=2)
         o, lse = _run(fa, a, naive=True)
-        o_ref, lse_ref = run_oracle(a)
-        compare(o, None, o_ref, None, tol_o=2e-2, tol_rel=1e-2)
+        o_ref, lse_ref, a_ref = run_oracle(a)
+        compare(o, None, o_ref, None, a_ref, tol_o=2e-2, tol_rel=1e-2)
         bound = naive_lse_bound(a)
         fin = np.isfinite(lse_ref)
         assert np.array_equal(np.isneginf(lse), ~fin)
@@ -140,6 +139,6 @@ def test_naive_matches_oracle(fa):
 def test_naive_one_head_n8192(fa):
     a = I.make_workload("one_head_n8192_d128")
     o, lse = _run(fa, a, naive=True)
-    o_ref, lse_ref = run_oracle(a)
-    compare(o, None, o_ref, None, tol_o=2e-2, tol_rel=1e-2)
+    o_ref, lse_ref, a_ref = run_oracle(a)
+    compare(o, None, o_ref, None, a_ref, tol_o=2e-2, tol_rel=1e-2)
     assert np.all(np.abs(lse - lse_ref) <= naive_lse_bound(a))
