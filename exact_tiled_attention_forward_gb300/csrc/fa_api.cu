@@ -201,6 +201,106 @@ int* device_status_ptr() {
   return ptrs[dev];
 }
 
+namespace {
+
+int pool_acquire(size_t bytes, cudaStream_t stream, void** ptr) {
+  cudaMemPool_t pool = workspace_pool();
+  if (!pool) return cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = (int)e;
+    return FA_ERR_NO_MEMORY;
+  }
+  return FA_OK;
+}
+
+void pool_release(void* ptr, cudaStream_t stream) { cudaFreeAsync(ptr, stream); }
+
+}  // namespace
+
+const WorkspaceSource& pool_workspace() {
+  static const WorkspaceSource src{pool_acquire, pool_release};
+  return src;
+}
+
+int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                 int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t strm,
+                 const WorkspaceSource& wsrc) {
+  const Shape s{B, H_q, H_kv, N_q, N_k, d};
+  int st = validate(q, k, v, o, lse, s, scale);
+  if (st != FA_OK) return st;
+  if ((long long)B * H_q * N_q == 0) return FA_OK;
+  if (N_k == 0 || B * H_kv == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
+
+  int* status = device_status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  const int G = H_q / H_kv;
+  CUtensorMap tk, tv;
+  if (!make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
+      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  if ((long long)G * N_q <= kDecodeMaxRows) {
+    // decode / few queries: every query row of a KV head fits one m16 MMA
+    DecParams p{};
+    p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+    p.G = G; p.R = G * N_q;
+    p.causal = causal ? 1 : 0;
+    p.kv_off = N_k - N_q;
+    p.n_chunks = (N_k + 127) / 128;
+    p.c = scale * 1.4426950408889634f;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.o = o;
+    p.lse = lse;
+    p.status = status;
+    if ((long long)B * H_kv * p.n_chunks >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    const size_t bytes = decode_part_bytes(B, H_kv, p.R, p.n_chunks, d);
+    void* ws = nullptr;
+    st = wsrc.acquire(bytes, strm, &ws);
+    if (st != FA_OK) return st;
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                         (size_t)B * H_kv * p.n_chunks * p.R * d * 4);
+    cudaError_t e = launch_decode(d, tk, tv, p, strm);
+    if (wsrc.release) wsrc.release(ws, strm);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
+
+  FwdParams p{};
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+  p.causal = causal ? 1 : 0;
+  p.kv_off = N_k - N_q;
+  p.n_qb = (N_q + kBlockRows - 1) / kBlockRows;
+  p.n_kv_tiles = (N_k + kTileN - 1) / kTileN;
+  p.c = scale * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  const long long blocks = (long long)B * H_q * p.n_qb;
+  // causal blocks see on average about half the key tiles
+  const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
+  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
+  if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  p.u_full = pl.u_full;
+  p.n_tail = pl.n_tail;
+  p.s_tail = pl.s_tail;
+
+  CUtensorMap tq;
+  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128))
+    return cuda_fail(cudaErrorInvalidValue);
+  void* ws = nullptr;
+  if (pl.n_tail > 0) {
+    st = wsrc.acquire(pl.part_bytes, strm, &ws);
+    if (st != FA_OK) return st;
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                         (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
+  }
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)pl.units, strm);
+  if (ws && wsrc.release) wsrc.release(ws, strm);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -248,58 +348,8 @@ size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k) {
 
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream) {
-  const Shape s{B, H_q, H_kv, N_q, N_k, d};
-  int st = validate(q, k, v, o, lse, s, scale);
-  if (st != FA_OK) return st;
-  if ((long long)B * H_q * N_q == 0) return FA_OK;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  if (N_k == 0 || B * H_kv == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
-
-  int* status = device_status_ptr();
-  if (!status) return cuda_fail(cudaGetLastError());
-
-  FwdParams p{};
-  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
-  p.causal = causal ? 1 : 0;
-  p.kv_off = N_k - N_q;
-  p.n_qb = (N_q + kBlockRows - 1) / kBlockRows;
-  p.n_kv_tiles = (N_k + kTileN - 1) / kTileN;
-  p.c = scale * 1.4426950408889634f;
-  p.o = o;
-  p.lse = lse;
-  p.status = status;
-  const long long blocks = (long long)B * H_q * p.n_qb;
-  // causal blocks see on average about half the key tiles
-  const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
-  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
-  if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-  p.u_full = pl.u_full;
-  p.n_tail = pl.n_tail;
-  p.s_tail = pl.s_tail;
-  const long long units = pl.units;
-
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
-      !make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
-      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128))
-    return cuda_fail(cudaErrorInvalidValue);
-
-  void* ws = nullptr;
-  if (pl.n_tail > 0) {
-    cudaMemPool_t pool = workspace_pool();
-    if (!pool) return cuda_fail(cudaGetLastError());
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.part_bytes, pool, strm);
-    if (e != cudaSuccess) {
-      g_last_cuda_error = (int)e;
-      return FA_ERR_NO_MEMORY;
-    }
-    p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                         (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
-  }
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)units, strm);
-  if (ws) cudaFreeAsync(ws, strm);
-  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
+                      static_cast<cudaStream_t>(stream), pool_workspace());
 }
 
 int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -1,0 +1,374 @@
+// Decode / few-query attention forward for sm_103a ("FlashAttention HBM bytes,
+// one head, 8K", "What interviewers probe next": one query against many keys
+// is bandwidth-bound — K and V are read once per KV head — and "Why is
+// standard attention memory-bound...", "Does FlashAttention help when
+// generating one token at a time?": split the key sequence across thread
+// blocks and combine).
+//
+// Work unit = (batch, KV head, chunk of 128 keys). The rows of a unit are all
+// query rows that read this KV head: R = G * N_q <= 16 (G = H_q / H_kv, GQA),
+// which is exactly the M = 16 of one mma.sync m16n8k16 — the contraction is a
+// real (16 x d) x (d x keys) product, tiny next to the K/V stream it rides on.
+//   * one thread issues two TMA loads (K tile, V tile; 128-byte swizzle) into
+//     shared memory on two mbarriers; 64 KB per CTA at d = 128 lets three CTAs
+//     share an SM, so one CTA's loads overlap the others' arithmetic;
+//   * each of the 4 warps takes 32 keys: S = Q K^T (Q fragments from global,
+//     K fragments by ldmatrix), an exact softmax over its 32 keys (max, exp2 of
+//     the folded scale, sum via quad shuffles), P kept in registers as the A
+//     operand of O = P V (V fragments by ldmatrix.trans);
+//   * the 4 warps' (m, l, O) are merged in shared memory into one partial per
+//     (row, chunk); fa_decode_merge_kernel merges the chunks of each row.
+// The kernel is bound by HBM bandwidth: algorithmic bytes are K and V once per
+// KV head, Q read and O, LSE written once.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr int kDecKeys = 128;   // keys per chunk (one CTA)
+constexpr float kLn2d = 0.6931471805599453f;
+
+template <int D>
+struct DecCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kBoxBytes = kDecKeys * 128;          // 128 keys x 128 bytes
+  static constexpr int kTileBytes = kDecKeys * D * 2;       // K or V chunk
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffMl = 2 * kTileBytes;             // [4 warps][16 rows][2] f32
+  static constexpr int kOffBar = kOffMl + 4 * 16 * 2 * 4;
+  static constexpr int kSmemBytes = kOffBar + 16 + 1024;
+  // merge buffer [4 warps][16 rows][D] f32 reuses the K tile (dead after S = Q K^T)
+  static_assert(4 * 16 * D * 4 <= kTileBytes, "merge buffer must fit in the K tile");
+};
+
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Byte address of element row `key`, 16-byte chunk `ch16` (of d) in a TMA tile
+// stored as 64-column boxes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_addr(uint32_t base, int key, int ch16) {
+  const int box = ch16 >> 3, ch = ch16 & 7;
+  return base + (uint32_t)(box * (kDecKeys * 128) + key * 128 + ((ch ^ (key & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const DecParams p) {
+  using C = DecCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t barK = sb + C::kOffBar, barV = sb + C::kOffBar + 8;
+  volatile int abort_flag = 0;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int chunk = blockIdx.x % p.n_chunks;
+  const int bhk = blockIdx.x / p.n_chunks;
+  const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
+  const int key0 = chunk * kDecKeys;
+
+  if (threadIdx.x == 0) {
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(barK, C::kTileBytes);
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxes; ++bx)
+      tma_load_3d(sb + C::kOffK + bx * C::kBoxBytes, &tmK, barK, bx * 64, key0, bhk);
+    mbar_arrive_expect_tx(barV, C::kTileBytes);
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxes; ++bx)
+      tma_load_3d(sb + C::kOffV + bx * C::kBoxBytes, &tmV, barV, bx * 64, key0, bhk);
+  }
+
+  // Q fragments (A operand, rows = the R query rows of this KV head, zero-padded to 16)
+  uint32_t qa[D / 16][4];
+  {
+    const int rows[2] = {g, g + 8};
+    const uint32_t* qrow[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int m = rows[u];
+      if (m < p.R) {
+        const int hl = m / p.N_q, i = m - hl * p.N_q;
+        const int hq = hk * p.G + hl;
+        qrow[u] = reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * p.H_q + hq) * p.N_q + i) * D);
+      } else {
+        qrow[u] = nullptr;
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qa[ks][0] = qrow[0] ? __ldg(qrow[0] + ks * 8 + t) : 0u;
+      qa[ks][1] = qrow[1] ? __ldg(qrow[1] + ks * 8 + t) : 0u;
+      qa[ks][2] = qrow[0] ? __ldg(qrow[0] + ks * 8 + 4 + t) : 0u;
+      qa[ks][3] = qrow[1] ? __ldg(qrow[1] + ks * 8 + 4 + t) : 0u;
+    }
+  }
+
+  const int kw = warp * 32;  // this warp's 32 keys within the chunk
+  bool ok = mbar_wait(barK, 0, &abort_flag, p.status);
+  // ---- S = Q K^T for 32 keys: 4 n-tiles of 8 keys
+  float sacc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+  if (ok) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {   // pairs of n-tiles
+        const int i = lane >> 3, rr = lane & 7;
+        const int key = kw + 16 * np + 8 * (i >> 1) + rr;
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(sw128_addr(sb + C::kOffK, key, 2 * ks + (i & 1)), b00, b01, b10, b11);
+        mma16816(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
+        mma16816(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+      }
+    }
+  }
+  // ---- exact softmax over this warp's 32 keys, rows g and g + 8
+  const float c = p.c;
+  float mrow[2], lrow[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int m = g + 8 * u;
+    const int i = (m < p.R) ? m % p.N_q : 0;
+    int lim = p.N_k - key0;                                  // keys of this chunk that exist
+    if (p.causal) lim = min(lim, i + p.kv_off + 1 - key0);   // ... and that row i may see
+    if (m >= p.R) lim = 0;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kw + 8 * nt + 2 * t + e;
+        float& sv = sacc[nt][2 * u + e];
+        if (key >= lim) sv = -INFINITY;
+        mx = fmaxf(mx, sv);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mb = (mx == -INFINITY) ? 0.f : mx * c;
+    float l = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float& sv = sacc[nt][2 * u + e];
+        sv = ex2_approx(fmaf(sv, c, -mb));
+        l += sv;
+      }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    mrow[u] = (mx == -INFINITY) ? -INFINITY : mb;   // scaled log2 units
+    lrow[u] = l;
+  }
+  // P as the A operand of O = P V: k-step j covers keys kw + 16j .. kw + 16j + 15
+  uint32_t pa[2][4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    pa[j][0] = pack_bf16x2(sacc[2 * j][0], sacc[2 * j][1]);
+    pa[j][1] = pack_bf16x2(sacc[2 * j][2], sacc[2 * j][3]);
+    pa[j][2] = pack_bf16x2(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
+    pa[j][3] = pack_bf16x2(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+  }
+  // ---- O = P V: D/8 n-tiles of 8 columns
+  float oacc[D / 8][4];
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[dn][e] = 0.f;
+  if (ok) ok = mbar_wait(barV, 0, &abort_flag, p.status);
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {   // pairs of d n-tiles
+        const int i = lane >> 3, rr = lane & 7;
+        const int key = kw + 16 * j + 8 * (i & 1) + rr;
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4_t(sw128_addr(sb + C::kOffV, key, 2 * dp + (i >> 1)), b00, b01, b10, b11);
+        mma16816(oacc[2 * dp], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b00, b01);
+        mma16816(oacc[2 * dp + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b10, b11);
+      }
+    }
+  } else {
+    // a load never arrived: wait (bounded) for any copy in flight before the CTA exits
+    volatile int never = 0;
+    mbar_wait(barK, 0, &never, p.status);
+    mbar_wait(barV, 0, &never, p.status);
+  }
+
+  // ---- merge the 4 warps' partials in shared memory (the K tile is dead now)
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(smem + C::kOffK);   // [4][16][D]
+  float* mml = reinterpret_cast<float*>(smem + C::kOffMl); // [4][16][2]
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int m = g + 8 * u;
+    float* dst = mo + ((size_t)warp * 16 + m) * D;
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn)
+      *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][2 * u], oacc[dn][2 * u + 1]);
+    if (t == 0) {
+      mml[(warp * 16 + m) * 2 + 0] = mrow[u];
+      mml[(warp * 16 + m) * 2 + 1] = lrow[u];
+    }
+  }
+  __syncthreads();
+  // each partial row: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w 2^(m_w - M) O_w
+  const size_t pbase = ((size_t)bhk * p.n_chunks + chunk) * p.R;
+  for (int idx = threadIdx.x; idx < p.R * D; idx += kDecThreads) {
+    const int m = idx / D, dcol = idx - m * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (mml[(w * 16 + m) * 2 + 1] > 0.f) M = fmaxf(M, mml[(w * 16 + m) * 2]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float lw = mml[(w * 16 + m) * 2 + 1];
+      if (lw > 0.f) {
+        const float wt = ex2_approx(mml[(w * 16 + m) * 2] - M);
+        L += wt * lw;
+        acc += wt * mo[((size_t)w * 16 + m) * D + dcol];
+      }
+    }
+    __stcg(p.part_o + (pbase + m) * D + dcol, acc);
+    if (dcol == 0) __stcg(reinterpret_cast<float2*>(p.part_ml) + pbase + m, make_float2(L > 0.f ? M : -INFINITY, L));
+  }
+}
+
+// Merge of the chunk partials of each query row (same algebra as the prefill
+// merge): one warp per row; lanes stride over chunks for (m, l) and over
+// columns for O.
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kCols = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long wrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long n_rows = (long long)p.B * p.H_kv * p.R;
+  if (wrow >= n_rows) return;
+  const int bhk = (int)(wrow / p.R), m = (int)(wrow % p.R);
+  const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
+  const int hl = m / p.N_q, i = m - hl * p.N_q;
+  const int hq = hk * p.G + hl;
+  const size_t stride = (size_t)p.R;                     // between chunks of one row
+  const size_t base = (size_t)bhk * p.n_chunks * p.R + m;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float M = -INFINITY;
+  for (int ch = lane; ch < p.n_chunks; ch += 32) {
+    const float2 v = __ldcg(ml + base + ch * stride);
+    if (v.y > 0.f) M = fmaxf(M, v.x);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+  float acc[kCols];
+#pragma unroll
+  for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int ch = 0; ch < p.n_chunks; ++ch) {
+    const float2 v = __ldcg(ml + base + ch * stride);
+    if (!(v.y > 0.f)) continue;
+    const float w = ex2_approx(v.x - M);
+    L += w * v.y;
+    const float* src = p.part_o + (base + ch * stride) * D + lane * kCols;
+    if constexpr (kCols == 4) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+    } else {
+      const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
+      acc[0] += w * a.x; acc[1] += w * a.y;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)b * p.H_q + hq) * p.N_q + i) * D;
+  if constexpr (kCols == 4) {
+    uint2 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(orow + lane * 4) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0 && p.lse)
+    p.lse[((size_t)b * p.H_q + hq) * p.N_q + i] = L > 0.f ? (M + __log2f(L)) * kLn2d : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
+                            cudaStream_t stream) {
+  using C = DecCfg<D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const long long ctas = (long long)p.B * p.H_kv * p.n_chunks;
+  fa_decode_kernel<D><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)p.B * p.H_kv * p.R;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_decode_merge_kernel<D>, p);
+}
+
+}  // namespace
+
+size_t decode_part_bytes(int B, int H_kv, int R, int n_chunks, int d) {
+  return (size_t)B * H_kv * n_chunks * R * ((size_t)d * 4 + 8);
+}
+
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
+                          cudaStream_t stream) {
+  if ((long long)p.B * p.H_kv * p.n_chunks <= 0) return cudaSuccess;
+  return d == 128 ? launch_decode_t<128>(tk, tv, p, stream) : launch_decode_t<64>(tk, tv, p, stream);
+}
+
+}  // namespace fa

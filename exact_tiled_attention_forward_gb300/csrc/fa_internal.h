@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -46,6 +47,27 @@ size_t fwd_smem_bytes(int d);
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int units, cudaStream_t stream);
 
+// ---- decode / few queries per KV head -------------------------------------------------
+constexpr int kDecodeMaxRows = 16;   // R = G * N_q rows per KV head must fit one m16 MMA
+
+struct DecParams {
+  int B, H_q, H_kv, N_q, N_k;
+  int G, R;          // G = H_q / H_kv; R = G * N_q query rows per (batch, KV head)
+  int causal, kv_off;
+  int n_chunks;      // ceil(N_k / 128)
+  float c;           // scale * log2(e)
+  const __nv_bfloat16* q;  // [B][H_q][N_q][d]
+  void* o;
+  float* lse;
+  float* part_o;     // fp32 [B*H_kv][n_chunks][R][d]
+  float* part_ml;    // fp32 [B*H_kv][n_chunks][R][2]
+  int* status;
+};
+size_t decode_part_bytes(int B, int H_kv, int R, int n_chunks, int d);
+// Launch the decode kernel, then the chunk merge as its programmatic dependent.
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
+                          cudaStream_t stream);
+
 // ---- unfused baseline -------------------------------------------------------------
 struct GemmParams {
   int M, N, K;          // per batch: C[M][N] = alpha * A[M][K] * B
@@ -88,5 +110,18 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint6
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);
 
 int* device_status_ptr();   // address of the current device's status word (nullptr on error)
+
+// Where a forward call gets its split / decode partials from. acquire returns
+// FA_OK with *ptr set, or an fa_status code (nothing enqueued); release is
+// called (stream-ordered) after the kernels that use the memory.
+struct WorkspaceSource {
+  int (*acquire)(size_t bytes, cudaStream_t stream, void** ptr);
+  void (*release)(void* ptr, cudaStream_t stream);
+};
+const WorkspaceSource& pool_workspace();   // library-owned stream-ordered pool
+// The whole fused forward (validation, decode or prefill plan, launches).
+int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                 int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t stream,
+                 const WorkspaceSource& ws);
 
 }  // namespace fa

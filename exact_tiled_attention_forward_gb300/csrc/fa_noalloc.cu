@@ -1,6 +1,6 @@
 // fa_forward_noalloc: the fused forward for callers that cannot allocate device
-// memory. Same kernel and same work split as fa_forward; the only difference is
-// where the split-key partials live. fa_forward takes them from a
+// memory. Same kernels and same work split as fa_forward; the only difference
+// is where the split-key and decode partials live. fa_forward takes them from a
 // stream-ordered pool; this entry point uses a fixed array that is part of the
 // library's own device image, so no call ever allocates.
 //
@@ -17,12 +17,13 @@
 namespace fa {
 namespace {
 
-// Scratch for the split-key partials: per split CTA, kBlockRows rows of FP32
-// O (d values) plus (m, l). 32 MiB holds up to 252 split CTAs at d = 128
-// (the 1-head N = 8192 workload uses 128 of them, 17 MiB). Every GPU that
+// Scratch for the partials: per split prefill CTA, kBlockRows rows of FP32
+// O (d values) plus (m, l); per decode chunk, R rows of the same. 32 MiB holds
+// up to 252 split CTAs at d = 128 (the 1-head N = 8192 workload uses 128 of
+// them, 17 MiB; batch-16 decode over 8192 keys uses 17 MiB). Every GPU that
 // loads libfa holds this array until the process exits. Nothing in it needs
-// to start at zero: every partial row the merge reads is written first by
-// the same call.
+// to start at zero: every partial row a merge reads is written first by the
+// same call.
 constexpr size_t kScratchBytes = 32u << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -54,52 +55,26 @@ void* scratch_address(int* err) {
 
 using namespace fa;
 
+namespace fa {
+namespace {
+
+int scratch_acquire(size_t bytes, cudaStream_t, void** ptr) {
+  if (bytes > kScratchBytes) return FA_ERR_TOO_LARGE;
+  int err = 0;
+  void* base = scratch_address(&err);
+  if (!base) return cuda_fail((cudaError_t)err);
+  *ptr = base;
+  return FA_OK;
+}
+
+const WorkspaceSource kScratchSource{scratch_acquire, nullptr};
+
+}  // namespace
+}  // namespace fa
+
 extern "C" int fa_forward_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
                                   float scale, void* stream) {
-  const Shape s{B, H_q, H_kv, N_q, N_k, d};
-  int st = validate(q, k, v, o, lse, s, scale);
-  if (st != FA_OK) return st;
-  if ((long long)B * H_q * N_q == 0) return FA_OK;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  if (N_k == 0 || B * H_kv == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
-
-  int* status = device_status_ptr();
-  if (!status) return cuda_fail(cudaGetLastError());
-
-  FwdParams p{};
-  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
-  p.causal = causal ? 1 : 0;
-  p.kv_off = N_k - N_q;
-  p.n_qb = (N_q + kBlockRows - 1) / kBlockRows;
-  p.n_kv_tiles = (N_k + kTileN - 1) / kTileN;
-  p.c = scale * 1.4426950408889634f;
-  p.o = o;
-  p.lse = lse;
-  p.status = status;
-  const long long blocks = (long long)B * H_q * p.n_qb;
-  const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
-  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
-  if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-  p.u_full = pl.u_full;
-  p.n_tail = pl.n_tail;
-  p.s_tail = pl.s_tail;
-  const long long units = pl.units;
-
-  if (pl.n_tail > 0) {
-    if (pl.part_bytes > kScratchBytes) return FA_ERR_TOO_LARGE;
-    int err = 0;
-    char* base = static_cast<char*>(scratch_address(&err));
-    if (!base) return cuda_fail((cudaError_t)err);
-    p.part_o = reinterpret_cast<float*>(base);
-    p.part_ml = reinterpret_cast<float*>(base + (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
-  }
-
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
-      !make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
-      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128))
-    return cuda_fail(cudaErrorInvalidValue);
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)units, strm);
-  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
+                      static_cast<cudaStream_t>(stream), kScratchSource);
 }

@@ -57,11 +57,13 @@ typedef enum {
 } fa_status;
 
 /* Exact attention forward, fused (the tiled online-softmax kernel).
- * Prefill (N_q > 1 or B*H_q large): tcgen05/TMA kernel, two 128-row query
- * tiles per CTA, K/V tiles of 128 keys. Query blocks that do not fill a whole
- * wave of the GPU have their key range split over several CTAs; a second
- * kernel (programmatic dependent launch on the same stream) merges the
- * partial (m, l, O) results.
+ * Prefill: tcgen05/TMA kernel, two 128-row query tiles per CTA, K/V tiles of
+ * 128 keys. Query blocks that do not fill a whole wave of the GPU have their
+ * key range split over several CTAs; a second kernel (programmatic dependent
+ * launch on the same stream) merges the partial (m, l, O) results.
+ * Decode / few queries (the H_q/H_kv * N_q query rows that share a KV head
+ * number at most 16): one CTA per (batch, KV head, 128-key chunk) reads its
+ * K and V chunk once for all those rows; chunk partials are merged the same way.
  * Split and decode partials live in a stream-ordered workspace taken from a
  * library-owned memory pool on the current device (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`); the pool keeps freed memory reserved for later

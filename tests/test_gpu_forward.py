@@ -53,6 +53,13 @@ SMALL = [
     (1, 2, 1, 1000, 1000, 128, False),
     (3, 4, 1, 64, 1000, 128, False),    # GQA group 4
     (1, 1, 1, 1, 5000, 128, False),     # one query row, long key range
+    # decode path: G * N_q <= 16 rows per KV head
+    (2, 8, 2, 4, 777, 128, True),       # GQA 4 x 4 queries = 16 rows, ragged chunk
+    (1, 16, 1, 1, 300, 64, False),      # MQA, 16 heads on one KV head
+    (2, 4, 4, 3, 130, 128, True),       # 3 queries, causal, just past one chunk
+    (1, 2, 2, 16, 16, 64, True),        # square causal inside one chunk
+    (1, 2, 1, 8, 5, 128, True),         # N_q > N_k: leading rows see no key
+    (3, 8, 8, 1, 128, 128, False),      # exactly one chunk
 ]
 
 
