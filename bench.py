@@ -38,8 +38,10 @@ from exact_tiled_attention_forward_gb300 import work as W  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofline"
 DEFAULT_WORKLOAD = "one_head_n8192_d128"
+DECODE_WORKLOAD = "decode_b16_h32_kv8_n8192_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
+                  "exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
                   "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"]
 
 
@@ -60,10 +62,10 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    or None if there is none or the kernel source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None if there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -227,6 +229,60 @@ def cpu_oracle_throughput(a, budget_s: float, max_rows: int | None = None):
     return done_rows, dt, cores, calls
 
 
+def fused_launches_per_step(cfg, sms: int) -> int:
+    """Kernels one fa_forward call launches (mirrors libfa's work planner): the
+    decode or prefill kernel, plus the merge kernel when partials are split."""
+    G = cfg["H_q"] // cfg["H_kv"]
+    if G * cfg["N_q"] <= 16:
+        return 2  # decode kernel + chunk merge
+    n_qb = (cfg["N_q"] + 255) // 256
+    n_kv = (cfg["N_k"] + 127) // 128
+    kv_eff = (n_kv + 1) // 2 if cfg["causal"] else n_kv
+    blocks = cfg["B"] * cfg["H_q"] * n_qb
+    if kv_eff <= 1:
+        return 1
+    tail = blocks if blocks < sms else (0 if cfg["causal"] else blocks % sms)
+    if tail == 0:
+        return 1
+    best, best_cost = 1, 1e30
+    for sp in range(1, min(16, kv_eff) + 1):
+        waves = (tail * sp + sms - 1) // sms
+        cost = waves * (2.0 + kv_eff / sp) + (0.5 if sp > 1 else 0.0)
+        if cost < best_cost - 1e-9:
+            best, best_cost = sp, cost
+    return 2 if best > 1 else 1
+
+
+def time_decode(fa, torch, dev, flush, stream, steps, warmup, world):
+    """Device time of the decode workload (L2 flushed before each step); GB/s of
+    algorithmic bytes (K, V once per KV head, Q read, O and LSE written)."""
+    cfg, _, a_bytes, _ = workload_config(DECODE_WORKLOAD)
+    a = I.make_workload(DECODE_WORKLOAD)
+    to = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = to(a.q), to(a.k), to(a.v)
+    B, Hq, Hkv, Nq, Nk, d = a.shape_args
+    o = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        flush.zero_()
+        fa.fa_forward(q, k, v, causal=False, scale=a.scale, out=o, lse=lse)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fa.fa_forward(q, k, v, causal=False, scale=a.scale, out=o, lse=lse)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"ms": ms, "gbs": world * a_bytes / 1e9 / (ms * 1e-3), "bytes": a_bytes}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -234,6 +290,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fused", choices=["fused", "naive", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--decode-steps", type=int, default=200,
+                    help="timed steps of the decode workload reported beside the prefill line")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of host time for the cpu_baseline leg (0 disables it)")
     args = ap.parse_args()
@@ -241,9 +299,9 @@ def main():
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    cfg, a_flops, a_bytes, decode = workload_config(args.workload)
-    unit = "GB/s" if decode else "TFLOP/s"
-    work_per_step = (a_bytes / 1e9) if decode else (a_flops / 1e12)
+    cfg, a_flops, a_bytes, decode_cfg = workload_config(args.workload)
+    unit = "GB/s" if decode_cfg else "TFLOP/s"
+    work_per_step = (a_bytes / 1e9) if decode_cfg else (a_flops / 1e12)
 
     if args.impl == "reference":
         # The oracle on the host cores, rank 0 only; other ranks exit without work.
@@ -299,7 +357,8 @@ def main():
     ws = None
     if args.impl == "naive":
         ws = torch.empty(fa.fa_naive_workspace_bytes(B, Hq, Nq, Nk), dtype=torch.uint8, device=dev)
-    kernels_per_step = 3 if args.impl == "naive" else 1
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kernels_per_step = 3 if args.impl == "naive" else fused_launches_per_step(cfg, sms)
 
     def step(qq=q, kk=k, vv=v):
         if ws is None:
@@ -389,12 +448,17 @@ def main():
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
 
+    # ---- secondary half of the metric: decode HBM GB/s (batch 16, 32/8 heads, 8192 keys)
+    decode = None
+    if args.impl == "fused" and not decode_cfg and args.decode_steps > 0:
+        decode = time_decode(fa, torch, dev, flush, stream, args.decode_steps, warmup, world)
+
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
 
     peaks, peak_src = load_peaks()
-    if decode:
+    if decode_cfg:
         peak = float(peaks["hbm_gbs"])
         achieved = a_bytes / 1e9 / (ms_per_step * 1e-3)
         roof = {"bound": "hbm", "unit": "GB/s"}
@@ -405,7 +469,7 @@ def main():
     traffic = profiled_traffic(args.workload) if args.impl == "fused" else None
     roof.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
                  "traffic": traffic, "peak_source": f"{peak_src} (burst)",
-                 "algorithmic_per_launch": a_bytes if decode else a_flops,
+                 "algorithmic_per_launch": a_bytes if decode_cfg else a_flops,
                  "kernel": "fa_fwd_kernel" if args.impl == "fused" else "naive (3 kernels)"})
 
     cpu = None
@@ -430,6 +494,16 @@ def main():
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": kernels_per_step * args.steps,
+        "decode": None if decode is None else {
+            "workload": DECODE_WORKLOAD, "value": decode["gbs"], "unit": "GB/s",
+            "ms_per_step": decode["ms"], "steps": args.decode_steps,
+            "roofline": {"bound": "hbm", "achieved": decode["gbs"],
+                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": decode["gbs"] / float(peaks["hbm_gbs"]),
+                         "traffic": profiled_traffic(DECODE_WORKLOAD, "fa_decode_kernel"),
+                         "algorithmic_per_launch": decode["bytes"],
+                         "kernel": "fa_decode_kernel + fa_decode_merge_kernel"},
+            "gpu_launches": 2 * args.decode_steps},
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

@@ -274,16 +274,19 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 // Merge of the chunk partials of each query row (same algebra as the prefill
-// merge): one warp per row; lanes stride over chunks for (m, l) and over
-// columns for O.
+// merge). One CTA of D threads per row: the (m, l) of every chunk are turned
+// into weights 2^(m_c - M) / L once, in shared memory; then thread t sums
+// column t over the chunks with independent, coalesced loads.
+constexpr int kMergeMaxChunks = 1024;   // chunks merged per pass (longer rows loop)
+
 template <int D>
-__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecParams p) {
+__global__ void __launch_bounds__(D) fa_decode_merge_kernel(const DecParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int kCols = D / 32;
-  const int lane = threadIdx.x & 31;
-  const long long wrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const long long n_rows = (long long)p.B * p.H_kv * p.R;
-  if (wrow >= n_rows) return;
+  __shared__ float s_w[kMergeMaxChunks];
+  __shared__ float s_red[D / 32];
+  __shared__ float s_ML[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long wrow = blockIdx.x;
   const int bhk = (int)(wrow / p.R), m = (int)(wrow % p.R);
   const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
   const int hl = m / p.N_q, i = m - hl * p.N_q;
@@ -291,43 +294,63 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const DecParams p)
   const size_t stride = (size_t)p.R;                     // between chunks of one row
   const size_t base = (size_t)bhk * p.n_chunks * p.R + m;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  // pass 1: M = max over chunks with l > 0
   float M = -INFINITY;
-  for (int ch = lane; ch < p.n_chunks; ch += 32) {
+  for (int ch = tid; ch < p.n_chunks; ch += D) {
     const float2 v = __ldcg(ml + base + ch * stride);
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f;
-  float acc[kCols];
-#pragma unroll
-  for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int ch = 0; ch < p.n_chunks; ++ch) {
-    const float2 v = __ldcg(ml + base + ch * stride);
-    if (!(v.y > 0.f)) continue;
-    const float w = ex2_approx(v.x - M);
-    L += w * v.y;
-    const float* src = p.part_o + (base + ch * stride) * D + lane * kCols;
-    if constexpr (kCols == 4) {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    } else {
-      const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
-      acc[0] += w * a.x; acc[1] += w * a.y;
-    }
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  if (tid == 0) {
+    float mm = s_red[0];
+    for (int w = 1; w < D / 32; ++w) mm = fmaxf(mm, s_red[w]);
+    s_ML[0] = mm;
   }
+  __syncthreads();
+  M = s_ML[0];
+  float acc = 0.f, Lpart = 0.f;
+  const float* src = p.part_o + base * D + tid;
+  for (int c0 = 0; c0 < p.n_chunks; c0 += kMergeMaxChunks) {
+    const int nc = min(kMergeMaxChunks, p.n_chunks - c0);
+    // pass 2: unnormalised weights of this group of chunks
+    for (int ch = tid; ch < nc; ch += D) {
+      const float2 v = __ldcg(ml + base + (size_t)(c0 + ch) * stride);
+      const float w = (v.y > 0.f) ? ex2_approx(v.x - M) : 0.f;
+      s_w[ch] = w;
+      Lpart += w * v.y;
+    }
+    __syncthreads();
+    // pass 3: column tid; 32 independent loads in flight per step
+#pragma unroll 1
+    for (int g0 = 0; g0 < nc; g0 += 32) {
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        v[u] = (g0 + u < nc) ? __ldcg(src + (size_t)(c0 + g0 + u) * stride * D) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (g0 + u < nc) acc += s_w[g0 + u] * v[u];
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, off);
+  if (lane == 0) s_red[warp] = Lpart;
+  __syncthreads();
+  if (tid == 0) {
+    float L = 0.f;
+    for (int w = 0; w < D / 32; ++w) L += s_red[w];
+    s_ML[1] = L;
+  }
+  __syncthreads();
+  const float L = s_ML[1];
   const float inv = L > 0.f ? 1.f / L : 0.f;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)b * p.H_q + hq) * p.N_q + i) * D;
-  if constexpr (kCols == 4) {
-    uint2 v;
-    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(orow + lane * 4) = v;
-  } else {
-    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  }
-  if (lane == 0 && p.lse)
+  orow[tid] = __float2bfloat16_rn(acc * inv);
+  if (tid == 0 && p.lse)
     p.lse[((size_t)b * p.H_q + hq) * p.N_q + i] = L > 0.f ? (M + __log2f(L)) * kLn2d : -INFINITY;
 }
 
@@ -348,8 +371,8 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.H_kv * p.R;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(D);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -511,6 +511,22 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   if (row >= p.N_q) return;
   const int S = p.s_tail;
   const size_t base = (size_t)t * S * kBlockRows + r;  // partial row of split 0
+  // every load of the row is independent: issue them all, then combine
+  constexpr int kMaxS = 16;
+  float4 va[kMaxS];
+#pragma unroll
+  for (int s2 = 0; s2 < kMaxS; ++s2) {
+    va[s2] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s2 < S) {
+      const float* src = p.part_o + (base + (size_t)s2 * kBlockRows) * D + lane * kCols;
+      if constexpr (kCols == 4) {
+        va[s2] = __ldcg(reinterpret_cast<const float4*>(src));
+      } else {
+        const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src));
+        va[s2] = make_float4(t2.x, t2.y, 0.f, 0.f);
+      }
+    }
+  }
   float m = -INFINITY, l = 0.f;
   if (lane < S) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + (size_t)lane * kBlockRows);
@@ -530,16 +546,14 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   float acc[kCols];
 #pragma unroll
   for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int s2 = 0; s2 < S; ++s2) {
-    const float ws = __shfl_sync(0xffffffffu, w, s2) * inv;
-    const float* src = p.part_o + (base + (size_t)s2 * kBlockRows) * D + lane * kCols;
+#pragma unroll
+  for (int s2 = 0; s2 < kMaxS; ++s2) {
+    const float ws = __shfl_sync(0xffffffffu, w, s2) * inv;   // 0 for s2 >= S
+    acc[0] += ws * va[s2].x;
+    acc[1] += ws * va[s2].y;
     if constexpr (kCols == 4) {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-      acc[0] += ws * a.x; acc[1] += ws * a.y; acc[2] += ws * a.z; acc[3] += ws * a.w;
-    } else {
-      const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
-      acc[0] += ws * a.x; acc[1] += ws * a.y;
+      acc[2] += ws * va[s2].z;
+      acc[3] += ws * va[s2].w;
     }
   }
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N_q + row) * D;
