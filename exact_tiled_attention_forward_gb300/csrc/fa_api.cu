@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -124,6 +125,14 @@ cudaMemPool_t workspace_pool() {
 }
 
 }  // namespace
+
+// Cluster K/V multicast variant of the fused kernel: FA_MULTICAST=1 turns it on
+// for plans without split tails, 0 (default) keeps the plain kernel. Read at
+// every call, so a process can compare both.
+bool multicast_enabled() {
+  const char* e = getenv("FA_MULTICAST");
+  return e && e[0] == '1';
+}
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -284,10 +293,18 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.u_full = pl.u_full;
   p.n_tail = pl.n_tail;
   p.s_tail = pl.s_tail;
+  p.n_units = (int)pl.units;
+  const bool multicast = pl.n_tail == 0 && pl.units >= 2 && multicast_enabled();
 
   CUtensorMap tq;
   if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128))
     return cuda_fail(cudaErrorInvalidValue);
+  if (multicast) {
+    // each CTA of a pair fetches half the rows of every K/V tile
+    if (!make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 64) ||
+        !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 64))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
   void* ws = nullptr;
   if (pl.n_tail > 0) {
     st = wsrc.acquire(pl.part_bytes, strm, &ws);
@@ -296,7 +313,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                          (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
   }
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)pl.units, strm);
+  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)pl.units, multicast, strm);
   if (ws && wsrc.release) wsrc.release(ws, strm);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }

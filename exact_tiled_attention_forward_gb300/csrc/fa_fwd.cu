@@ -127,7 +127,55 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   mbar_wait(bar, parity, &never, status);
 }
 
-template <int D>
+// Query block and key-tile counts of work unit u (see the kernel's unit comment).
+struct UnitInfo {
+  int bh, qb, split, S, slot, lo, n0, n1, nmax;
+};
+__device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int u) {
+  UnitInfo ui;
+  int qlin;
+  if (u < p.u_full) {
+    qlin = u; ui.split = 0; ui.S = 1; ui.slot = -1;
+  } else {
+    const int v = u - p.u_full;
+    qlin = p.u_full + v / p.s_tail; ui.split = v % p.s_tail; ui.S = p.s_tail; ui.slot = v;
+  }
+  const int qr = qlin % p.n_qb;
+  ui.bh = qlin / p.n_qb;
+  ui.qb = p.causal ? (p.n_qb - 1 - qr) : qr;
+  const int q0 = ui.qb * kBlockRows;
+  // key tiles each query tile needs: [0, kv_hi); fully masked tiles are never visited
+  int kvh[2];
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    const int first = q0 + X * kTileM;
+    if (first >= p.N_q) {
+      kvh[X] = 0;
+    } else if (!p.causal) {
+      kvh[X] = p.n_kv_tiles;
+    } else {
+      const int last_key = min_i(first + kTileM - 1, p.N_q - 1) + p.kv_off;
+      kvh[X] = last_key < 0 ? 0 : min_i(p.n_kv_tiles, last_key / kTileN + 1);
+    }
+  }
+  const int n_all = max_i(kvh[0], kvh[1]);
+  ui.lo = (int)(((long long)ui.split * n_all) / ui.S);
+  const int hi = (int)(((long long)(ui.split + 1) * n_all) / ui.S);
+  ui.n0 = max_i(0, min_i(hi, kvh[0]) - ui.lo);
+  ui.n1 = max_i(0, min_i(hi, kvh[1]) - ui.lo);
+  ui.nmax = max_i(ui.n0, ui.n1);
+  return ui;
+}
+
+// MC (multicast): CTAs run in clusters of two (units u and u ^ 1). When both
+// units belong to the same head they share every K/V tile load: each CTA
+// fetches half the tile's rows once from L2 and multicasts them into both
+// CTAs' shared memory, and a stage is refilled only after both CTAs' MMAs have
+// released it (each MMA commit arrives on both CTAs' "empty" barriers). A
+// causal pair walks the union of its key ranges (the shorter unit only
+// releases the extra tiles). Single-GPU only: the tiles come from this GPU's
+// own memory.
+template <int D, bool MC>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -149,53 +197,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   // blocks are numbered head-major (a head's blocks are adjacent, so its K/V
   // stay in L2); causal blocks run longest first within a head.
   const int u = blockIdx.x;
-  int qlin, split, S, slot;
-  if (u < p.u_full) {
-    qlin = u; split = 0; S = 1; slot = -1;
-  } else {
-    const int v = u - p.u_full;
-    qlin = p.u_full + v / p.s_tail; split = v % p.s_tail; S = p.s_tail; slot = v;
-  }
-  const int qr = qlin % p.n_qb;
-  const int bh = qlin / p.n_qb;
-  const int qb = p.causal ? (p.n_qb - 1 - qr) : qr;
+  const bool idle = MC && u >= p.n_units;   // completes the last cluster only
+  const UnitInfo ui = unit_info(p, idle ? 0 : u);
+  const int bh = ui.bh, qb = ui.qb, slot = ui.slot, lo = ui.lo;
+  const int n0 = idle ? 0 : ui.n0, n1 = idle ? 0 : ui.n1;
+  const int nmax = idle ? 0 : ui.nmax;
   const int b = bh / p.H_q;
   const int h = bh - b * p.H_q;
   const int bhk = b * p.H_kv + h / (p.H_q / p.H_kv);
   const int q0 = qb * kBlockRows;
-
-  // key tiles each query tile needs: [0, kv_hi[X]); fully masked tiles are never visited
-  int kv_hi0, kv_hi1;
-  {
-    int kvh[2];
-#pragma unroll
-    for (int X = 0; X < 2; ++X) {
-      const int first = q0 + X * kTileM;
-      if (first >= p.N_q) {
-        kvh[X] = 0;
-      } else if (!p.causal) {
-        kvh[X] = p.n_kv_tiles;
-      } else {
-        const int last_key = min_i(first + kTileM - 1, p.N_q - 1) + p.kv_off;
-        kvh[X] = last_key < 0 ? 0 : min_i(p.n_kv_tiles, last_key / kTileN + 1);
+  // cluster pairing: share K/V loads with the partner unit if it is the same head
+  bool share = false;
+  int n_loop = nmax;        // key tiles this CTA loads and releases
+  const int rank = u & 1;
+  if (MC && !idle) {
+    const int partner = u ^ 1;
+    if (partner < p.n_units) {
+      const UnitInfo pi = unit_info(p, partner);
+      if (pi.bh == bh && pi.lo == lo) {
+        share = true;
+        n_loop = max_i(nmax, pi.nmax);
       }
     }
-    kv_hi0 = kvh[0];
-    kv_hi1 = kvh[1];
   }
-  const int n_all = max_i(kv_hi0, kv_hi1);
-  const int lo = (int)(((long long)split * n_all) / S);
-  const int hi = (int)(((long long)(split + 1) * n_all) / S);
-  const int n0 = max_i(0, min_i(hi, kv_hi0) - lo);
-  const int n1 = max_i(0, min_i(hi, kv_hi1) - lo);
-  const int nmax = max_i(n0, n1);
 
   // ---- set-up
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarFull + s), 1);
-      mbar_init(bar(C::kBarEmpty + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), share ? 2 : 1);   // both CTAs release a shared stage
     }
     mbar_init(bar(C::kBarS + 0), 1);
     mbar_init(bar(C::kBarS + 1), 1);
@@ -222,12 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (MC) cluster_sync();   // the partner's barriers exist before any multicast reaches them
 
-  if (warp >= 8) {
+  if (idle) {
+    // no work: only the cluster barriers and the teardown
+  } else if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (warp == kWarpProducer) {
       // ======================= TMA producer =======================
-      if (lane == 0 && nmax > 0) {
+      if (lane == 0 && n_loop > 0) {
         int issued = 0;  // K/V tile loads issued
         mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
 #pragma unroll
@@ -238,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bx * 64, q0 + X * kTileM, bh);
         const uint64_t pol = policy_evict_last();
         bool ok = true;
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = 0; j < n_loop && ok; ++j) {
           const int tile = lo + j;
 #pragma unroll
           for (int sel = 0; sel < 2; ++sel) {  // 0: K tile, 1: V tile
@@ -250,11 +284,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(bar(C::kBarFull + st), C::kTileBytes);
+            const void* tmap = sel ? (const void*)&tmV : (const void*)&tmK;
+            const uint32_t dst = sb + C::kOffKV + st * C::kTileBytes;
+            if (!MC) {
 #pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_3d_hint(sb + C::kOffKV + st * C::kTileBytes + bx * C::kBoxBytes,
-                               sel ? (const void*)&tmV : (const void*)&tmK, bar(C::kBarFull + st),
-                               bx * 64, tile * kTileN, bhk, pol);
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_3d_hint(dst + bx * C::kBoxBytes, tmap, bar(C::kBarFull + st), bx * 64,
+                                 tile * kTileN, bhk, pol);
+            } else if (share) {
+              // this CTA's half of the rows, into both CTAs
+#pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_3d_mc(dst + bx * C::kBoxBytes + rank * (kTileN / 2) * 128, tmap,
+                               bar(C::kBarFull + st), bx * 64, tile * kTileN + rank * (kTileN / 2),
+                               bhk, (uint16_t)0x3);
+            } else {
+#pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                  tma_load_3d_hint(dst + bx * C::kBoxBytes + hf * (kTileN / 2) * 128, tmap,
+                                   bar(C::kBarFull + st), bx * 64, tile * kTileN + hf * (kTileN / 2),
+                                   bhk, pol);
+            }
             ++issued;
           }
         }
@@ -268,7 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kWarpMma) {
       // ======================= tcgen05 MMA issuer =======================
-      if (lane == 0 && nmax > 0) {
+      if (lane == 0 && n_loop > 0) {
+        // a stage is released to this CTA's producer, and with sharing to the partner's too
+        auto release = [&](int st) {
+          if (share) mma_commit_mc(bar(C::kBarEmpty + st), (uint16_t)0x3);
+          else mma_commit(bar(C::kBarEmpty + st));
+        };
         constexpr uint32_t idS = idesc_bf16_f32(128, kTileN, false);
         constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
         // Descriptors are built once; each MMA adds a compile-time offset to the
@@ -305,14 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (n0 > 0) { issue_S(0, 0); mma_commit(bar(C::kBarS + 0)); }
           if (n1 > 0) { issue_S(1, 0); mma_commit(bar(C::kBarS + 1)); }
-          mma_commit(bar(C::kBarEmpty + 0));
+          release(0);
         }
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = 0; j < n_loop && ok; ++j) {
           const int itV = 2 * j + 1, itK = 2 * j + 2;
           const int stV = itV % C::kStages, stK = itK % C::kStages;
           const uint32_t phV = (uint32_t)(itV / C::kStages) & 1u;
           const uint32_t phK = (uint32_t)(itK / C::kStages) & 1u;
-          const bool next = (j + 1) < nmax;
+          const bool next = (j + 1) < n_loop;
           if (!(ok = mbar_wait(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
           tc_fence_after();
           if (j < n0) {
@@ -330,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_PV(1, stV, j > 0);
           }
-          mma_commit(bar(C::kBarEmpty + stV));
+          release(stV);
           if (next) {
             if (j + 1 < n1) { issue_S(1, stK); mma_commit(bar(C::kBarS + 1)); }
-            mma_commit(bar(C::kBarEmpty + stK));
+            release(stK);
           }
         }
         mma_commit(bar(C::kBarO));
@@ -486,6 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // neither CTA of a cluster exits while the other may still multicast into its
+  // shared memory or arrive on its barriers
+  if (MC) cluster_sync();
 }
 
 // Merge of the split-key partials (the online-softmax merge of page 2, "The
@@ -568,18 +628,40 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   if (lane == 0 && p.lse) p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
-template <int D>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, int units, cudaStream_t stream) {
+template <int D, bool MC>
+cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FwdParams& p, int units, cudaStream_t stream) {
   static bool attr = false;  // benign race: setting the attribute twice is harmless
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  fa_fwd_kernel<D><<<units, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  if (!MC) {
+    fa_fwd_kernel<D, false><<<units, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((units + 1) & ~1));   // whole clusters of two
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, true>, tq, tk, tv, p);
+}
+
+template <int D>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, int units, bool multicast, cudaStream_t stream) {
+  cudaError_t e = multicast ? launch_main_t<D, true>(tq, tk, tv, p, units, stream)
+                            : launch_main_t<D, false>(tq, tk, tv, p, units, stream);
   if (e != cudaSuccess || p.n_tail == 0) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(((long long)p.n_tail * kBlockRows + 7) / 8));
@@ -601,10 +683,10 @@ size_t fwd_smem_bytes(int d) {
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int units, cudaStream_t stream) {
+                       const FwdParams& p, int units, bool multicast, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  return d == 128 ? launch_fwd_t<128>(tq, tk, tv, p, units, stream)
-                  : launch_fwd_t<64>(tq, tk, tv, p, units, stream);
+  return d == 128 ? launch_fwd_t<128>(tq, tk, tv, p, units, multicast, stream)
+                  : launch_fwd_t<64>(tq, tk, tv, p, units, multicast, stream);
 }
 
 }  // namespace fa

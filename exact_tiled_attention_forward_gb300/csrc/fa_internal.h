@@ -23,6 +23,7 @@ struct FwdParams {
   int u_full;       // units [0, u_full) are whole query blocks (query blocks 0 .. u_full-1)
   int n_tail;       // query blocks u_full .. u_full+n_tail-1 are split ...
   int s_tail;       // ... into s_tail key ranges each (units u_full + t*s_tail + s)
+  int n_units;      // work units (the grid may hold one more, idle, CTA to complete a cluster)
   float c;          // scale * log2(e)
   void* o;          // bf16 [B][H_q][N_q][d]
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
@@ -43,9 +44,11 @@ FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms
 size_t fwd_smem_bytes(int d);
 
 // Launch the fused kernel over `units` CTAs, then (if p.n_tail > 0) the merge
-// kernel as its programmatic dependent on the same stream.
+// kernel as its programmatic dependent on the same stream. With multicast,
+// CTAs run in clusters of two that share K/V tile loads (no split plans;
+// tk / tv must then be built with 64-row boxes).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int units, cudaStream_t stream);
+                       const FwdParams& p, int units, bool multicast, cudaStream_t stream);
 
 // ---- decode / few queries per KV head -------------------------------------------------
 constexpr int kDecodeMaxRows = 16;   // R = G * N_q rows per KV head must fit one m16 MMA
