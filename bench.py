@@ -229,28 +229,10 @@ def cpu_oracle_throughput(a, budget_s: float, max_rows: int | None = None):
     return done_rows, dt, cores, calls
 
 
-def fused_launches_per_step(cfg, sms: int) -> int:
-    """Kernels one fa_forward call launches (mirrors libfa's work planner): the
-    decode or prefill kernel, plus the merge kernel when partials are split."""
-    G = cfg["H_q"] // cfg["H_kv"]
-    if G * cfg["N_q"] <= 16:
-        return 2  # decode kernel + chunk merge
-    n_qb = (cfg["N_q"] + 255) // 256
-    n_kv = (cfg["N_k"] + 127) // 128
-    kv_eff = (n_kv + 1) // 2 if cfg["causal"] else n_kv
-    blocks = cfg["B"] * cfg["H_q"] * n_qb
-    if kv_eff <= 1:
-        return 1
-    tail = blocks if blocks < sms else (0 if cfg["causal"] else blocks % sms)
-    if tail == 0:
-        return 1
-    best, best_cost = 1, 1e30
-    for sp in range(1, min(16, kv_eff) + 1):
-        waves = (tail * sp + sms - 1) // sms
-        cost = waves * (2.0 + kv_eff / sp) + (0.5 if sp > 1 else 0.0)
-        if cost < best_cost - 1e-9:
-            best, best_cost = sp, cost
-    return 2 if best > 1 else 1
+def fused_launches_per_step(fa, cfg) -> int:
+    """Kernels one fa_forward call launches (the library's own plan for it)."""
+    return fa.fa_forward_plan(cfg["B"], cfg["H_q"], cfg["H_kv"], cfg["N_q"], cfg["N_k"], cfg["d"],
+                              cfg["causal"])["launches"]
 
 
 def time_decode(fa, torch, dev, flush, stream, steps, warmup, world):
@@ -357,8 +339,7 @@ def main():
     ws = None
     if args.impl == "naive":
         ws = torch.empty(fa.fa_naive_workspace_bytes(B, Hq, Nq, Nk), dtype=torch.uint8, device=dev)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    kernels_per_step = 3 if args.impl == "naive" else fused_launches_per_step(cfg, sms)
+    kernels_per_step = 3 if args.impl == "naive" else fused_launches_per_step(fa, cfg)
 
     def step(qq=q, kk=k, vv=v):
         if ws is None:

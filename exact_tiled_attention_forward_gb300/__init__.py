@@ -51,6 +51,8 @@ _SIGNATURES = {
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
     "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
+    "fa_forward_plan": (_c_int, [_c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong),
+                                                ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_get_last_cuda_error": (_c_int, []),
     "fa_device_status": (_c_int, [_c_int]),
@@ -138,6 +140,18 @@ def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None
                                   N_q, N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "fa_forward_noalloc")
     return out, lse
+
+
+def fa_forward_plan(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int,
+                    causal: bool = False) -> dict:
+    """How fa_forward runs this request on the current device: CTAs of its main
+    kernel, kernels it launches, workspace bytes it allocates (the scratch that
+    fa_forward_noalloc needs)."""
+    ctas, launches, ws = ctypes.c_longlong(0), _c_int(0), _c_size(0)
+    st = lib().fa_forward_plan(B, H_q, H_kv, N_q, N_k, d, int(bool(causal)), ctypes.byref(ctas),
+                               ctypes.byref(launches), ctypes.byref(ws))
+    _check(st, "fa_forward_plan")
+    return {"ctas": int(ctas.value), "launches": int(launches.value), "workspace_bytes": int(ws.value)}
 
 
 def fa_naive_workspace_bytes(B: int, H_q: int, N_q: int, N_k: int) -> int:

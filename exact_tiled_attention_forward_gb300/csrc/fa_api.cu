@@ -54,17 +54,25 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 // Shared validation of the fa_forward / fa_naive_forward arguments.
-int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const Shape& s, float scale) {
+int validate_shape(const Shape& s) {
   if (s.B < 0 || s.N_q < 0 || s.N_k < 0 || s.H_q < 1 || s.H_kv < 1 || s.d < 1)
     return FA_ERR_INVALID_ARG;
   if (s.H_q % s.H_kv != 0) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   // indices inside the kernels are 32-bit per (batch*head) row
   const long long rows_q = (long long)s.B * s.H_q * s.N_q;
   const long long rows_k = (long long)s.B * s.H_kv * s.N_k;
   if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const Shape& s, float scale) {
+  int st = validate_shape(s);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const long long rows_q = (long long)s.B * s.H_q * s.N_q;
+  const long long rows_k = (long long)s.B * s.H_kv * s.N_k;
   if (rows_q == 0) return FA_OK;  // nothing to write
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return FA_ERR_INVALID_ARG;
@@ -134,6 +142,12 @@ bool multicast_enabled() {
   return e && e[0] == '1';
 }
 
+// In-cluster merge of split partials: on unless FA_CLUSTER_MERGE=0 (read at every call).
+bool cluster_merge_enabled() {
+  const char* e = getenv("FA_CLUSTER_MERGE");
+  return !(e && e[0] == '0');
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -144,18 +158,37 @@ int num_sms() {
 // Cut the query blocks into CTAs. Whole blocks fill complete waves of the
 // GPU; the blocks of an incomplete last wave (all blocks, when there are fewer
 // than one wave) have their key range split into s parts when that shortens
-// the tail, and a merge kernel combines the parts. Cost model, in key-tile
-// steps: waves * (2 + key tiles per part) + 0.5 for the merge. Causal
-// problems with at least a wave of blocks are not split: their blocks differ
-// in length and the in-order dispatch of longest-first blocks balances them.
-FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms) {
+// the tail. The parts are combined either by a merge kernel (partials through
+// the workspace) or, when every block is split, inside a cluster of the s CTAs
+// of each block (distributed shared memory, no workspace). Cost model, in
+// key-tile steps of one CTA: a wave costs 2 (set-up and epilogue) + its key
+// tiles; the merge kernel costs 3 more (its launch and the partials' round trip
+// through L2), the in-cluster merge 0.5. Causal problems with at least a wave
+// of blocks are not split: their blocks differ in length and the in-order
+// dispatch of longest-first blocks balances them.
+FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms, const int* cluster_cap) {
   FwdPlan pl{};
   pl.u_full = (int)blocks;
   pl.n_tail = 0;
   pl.s_tail = 1;
   pl.units = blocks;
   pl.part_bytes = 0;
+  pl.cluster_merge = 0;
   if (blocks <= 0 || kv_tiles <= 1 || sms <= 0) return pl;
+  // fewer blocks than SMs: split every block, merging inside clusters of s CTAs
+  int cm_s = 1;
+  double cm_cost = 2.0 + (double)kv_tiles;   // unsplit: one wave
+  if (blocks < sms && cluster_cap) {
+    for (int s = 2; s <= 8 && s <= kv_tiles; s *= 2) {   // s divides the block's 256 rows
+      if (cluster_cap[s] <= 0) continue;
+      const long long waves = (blocks + cluster_cap[s] - 1) / cluster_cap[s];
+      const double cost = (double)waves * (2.0 + (double)kv_tiles / s) + 0.5;
+      if (cost < cm_cost - 1e-9) {
+        cm_cost = cost;
+        cm_s = s;
+      }
+    }
+  }
   long long tail = 0;
   if (blocks < sms) {
     tail = blocks;
@@ -167,11 +200,19 @@ FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms
   double best_cost = 1e30;
   for (int s = 1; s <= 16 && s <= kv_tiles; ++s) {
     const long long waves = (tail * s + sms - 1) / sms;
-    const double cost = (double)waves * (2.0 + (double)kv_tiles / s) + (s > 1 ? 0.5 : 0.0);
+    const double cost = (double)waves * (2.0 + (double)kv_tiles / s) + (s > 1 ? 3.0 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
+  }
+  if (cm_s > 1 && cm_cost <= best_cost + 1e-9) {
+    pl.u_full = 0;
+    pl.n_tail = (int)blocks;
+    pl.s_tail = cm_s;
+    pl.units = blocks * cm_s;
+    pl.cluster_merge = 1;
+    return pl;
   }
   if (best == 1) return pl;
   pl.u_full = (int)(blocks - tail);
@@ -192,6 +233,19 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint6
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -230,6 +284,21 @@ void pool_release(void* ptr, cudaStream_t stream) { cudaFreeAsync(ptr, stream); 
 const WorkspaceSource& pool_workspace() {
   static const WorkspaceSource src{pool_acquire, pool_release};
   return src;
+}
+
+// The plan fa_forward uses for a prefill request on the current device.
+FwdPlan prefill_plan(int B, int H_q, int N_q, int N_k, int d, int causal) {
+  const int n_qb = (N_q + kBlockRows - 1) / kBlockRows;
+  const int n_kv = (N_k + kTileN - 1) / kTileN;
+  const long long blocks = (long long)B * H_q * n_qb;
+  // causal blocks see on average about half the key tiles
+  const int kv_eff = causal ? (n_kv + 1) / 2 : n_kv;
+  const int sms = num_sms();
+  int cap[9] = {0};
+  const bool cm_ok = cluster_merge_enabled() && blocks < sms;
+  if (cm_ok)
+    for (int s2 = 2; s2 <= 8; s2 *= 2) cap[s2] = fwd_cluster_capacity(d, s2);
+  return plan_forward(blocks, kv_eff, causal != 0, d, sms, cm_ok ? cap : nullptr);
 }
 
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
@@ -285,35 +354,42 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.o = o;
   p.lse = lse;
   p.status = status;
-  const long long blocks = (long long)B * H_q * p.n_qb;
-  // causal blocks see on average about half the key tiles
-  const int kv_eff = causal ? (p.n_kv_tiles + 1) / 2 : p.n_kv_tiles;
-  const FwdPlan pl = plan_forward(blocks, kv_eff, causal != 0, d, num_sms());
+  const FwdPlan pl = prefill_plan(B, H_q, N_q, N_k, d, causal);
   if (pl.units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   p.u_full = pl.u_full;
   p.n_tail = pl.n_tail;
   p.s_tail = pl.s_tail;
   p.n_units = (int)pl.units;
+  p.cm = pl.cluster_merge;
   const bool multicast = pl.n_tail == 0 && pl.units >= 2 && multicast_enabled();
 
-  CUtensorMap tq;
-  if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128))
+  FwdMaps maps{};
+  maps.k = tk;
+  maps.v = tv;
+  // O boxes: a 128-row query tile, or the 256 / s rows one CTA of a cluster finishes
+  const uint32_t o_box_rows = pl.cluster_merge ? (uint32_t)(kBlockRows / pl.s_tail) : 128u;
+  if (!make_tmap_bf16_3d(&maps.q, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
+      !make_tmap_bf16_3d(&maps.o, o, d, N_q, (uint64_t)B * H_q, d, o_box_rows))
     return cuda_fail(cudaErrorInvalidValue);
   if (multicast) {
     // each CTA of a pair fetches half the rows of every K/V tile
-    if (!make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 64) ||
-        !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 64))
+    if (!make_tmap_bf16_3d(&maps.k, k, d, N_k, (uint64_t)B * H_kv, d, 64) ||
+        !make_tmap_bf16_3d(&maps.v, v, d, N_k, (uint64_t)B * H_kv, d, 64))
       return cuda_fail(cudaErrorInvalidValue);
   }
   void* ws = nullptr;
-  if (pl.n_tail > 0) {
+  if (pl.part_bytes > 0) {
     st = wsrc.acquire(pl.part_bytes, strm, &ws);
     if (st != FA_OK) return st;
+    const uint64_t part_rows = (uint64_t)pl.n_tail * pl.s_tail * kBlockRows;
     p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                         (size_t)pl.n_tail * pl.s_tail * kBlockRows * d * 4);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + part_rows * d * 4);
+    if (!make_tmap_f32_2d(&maps.part, p.part_o, d, part_rows)) {
+      if (wsrc.release) wsrc.release(ws, strm);
+      return cuda_fail(cudaErrorInvalidValue);
+    }
   }
-  cudaError_t e = launch_fwd(d, tq, tk, tv, p, (int)pl.units, multicast, strm);
+  cudaError_t e = launch_fwd(d, maps, p, (int)pl.units, multicast, strm);
   if (ws && wsrc.release) wsrc.release(ws, strm);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -355,6 +431,37 @@ int fa_device_status(int reset) {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return h == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal, long long* ctas,
+                    int* launches, size_t* workspace_bytes) {
+  const fa::Shape s{B, H_q, H_kv, N_q, N_k, d};
+  int st = fa::validate_shape(s);
+  if (st != FA_OK) return st;
+  long long c = 0;
+  int n = 0;
+  size_t ws = 0;
+  if ((long long)B * H_q * N_q == 0) {
+    // nothing to compute
+  } else if (N_k == 0) {
+    c = 256;   // O = 0, LSE = -inf fill
+    n = 1;
+  } else if ((long long)(H_q / H_kv) * N_q <= fa::kDecodeMaxRows) {
+    const int chunks = (N_k + 127) / 128;
+    c = (long long)B * H_kv * chunks;
+    n = 2;
+    ws = fa::decode_part_bytes(B, H_kv, (H_q / H_kv) * N_q, chunks, d);
+  } else {
+    const fa::FwdPlan pl = fa::prefill_plan(B, H_q, N_q, N_k, d, causal);
+    c = pl.units;
+    if (pl.n_tail == 0 && pl.units >= 2 && fa::multicast_enabled()) c = (pl.units + 1) & ~1ll;
+    n = pl.part_bytes > 0 ? 2 : 1;
+    ws = pl.part_bytes;
+  }
+  if (ctas) *ctas = c;
+  if (launches) *launches = n;
+  if (workspace_bytes) *workspace_bytes = ws;
+  return FA_OK;
 }
 
 size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k) {

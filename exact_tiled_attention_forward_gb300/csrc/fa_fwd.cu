@@ -72,7 +72,13 @@ struct Cfg {
   static constexpr int kBarDrain = 6 + 2 * kStages;
   static constexpr int kNumBars = 7 + 2 * kStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  // in-cluster merge: (m, l) of up to kCmRows partial rows received from the
+  // cluster; their O rows land in [0, kOffBar) (the Q tiles and the K/V ring)
+  static constexpr int kCmRows = kBlockRows;                  // (m, l) of every row, by sender
+  static constexpr int kOffCm = (kOffMisc + 64 + 15) & ~15;
+  static constexpr int kCmStage = kBlockRows * D * 4;         // after the FP32 receive buffer
+  static constexpr int kSmemBytes = kOffCm + kCmRows * 8 + 1024;  // + alignment slack
+  static_assert(kCmStage + 128 * D * 2 <= kOffBar, "merge buffers must fit in the Q tiles and the K/V ring");
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory column of S_X / P_X and of O_X
   __device__ static constexpr uint32_t tm_s(int X) { return X ? 128u : 0u; }
@@ -127,6 +133,119 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   mbar_wait(bar, parity, &never, status);
 }
 
+// ---- in-cluster merge of the split partials (all query blocks split into S
+// key ranges, S in {2, 4, 8}; the S CTAs of a block form one cluster). Row rr
+// of the block (0..255) is finished by CTA rr / R, R = 256 / S: every CTA sends
+// its unnormalised FP32 O row and (m, l) there, and the owner combines the S
+// partials exactly as the merge of whole key ranges does (page 2, "The Tiling
+// Algorithm"). Distributed shared memory moves ~20 B/clk per SM at best, and
+// only when a warp's store covers contiguous bytes, so the receive buffer is
+// laid out [sender][16-byte chunk][row]: the 32 consecutive rows of a warp
+// write 512 contiguous bytes per store. Rows a CTA owns stay local.
+template <int D>
+__device__ __forceinline__ void cm_send(uint32_t sb, uint32_t ml_base, int S, int v, int rr, uint32_t tO,
+                                        int n, float m, float l) {
+  constexpr int kC = D / 4;               // 16-byte FP32 chunks per row
+  const int R = kBlockRows / S;
+  const int w = rr / R;                   // owner: the same for all 32 rows of a warp
+  const int lr = rr - w * R;
+  const uint32_t loc = sb + (uint32_t)(v * kC * R + lr) * 16u;   // chunk 0 of this row, slot v
+  const bool local = (w == v);
+  const uint32_t dst = local ? loc : mapa_shared(loc, (uint32_t)w);
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    float ov[32];
+    if (n > 0) {
+      tmem_ld32(tO + cc, ov);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t a = dst + (uint32_t)((cc / 4 + g) * R) * 16u;
+      const uint32_t x0 = __float_as_uint(ov[4 * g]), x1 = __float_as_uint(ov[4 * g + 1]);
+      const uint32_t x2 = __float_as_uint(ov[4 * g + 2]), x3 = __float_as_uint(ov[4 * g + 3]);
+      if (local) st_shared_v4(a, x0, x1, x2, x3);
+      else st_cluster_v4(a, x0, x1, x2, x3);
+    }
+  }
+  const uint32_t mla = ml_base + (uint32_t)(v * R + lr) * 8u;
+  st_cluster_v2f(local ? mla : mapa_shared(mla, (uint32_t)w), l > 0.f ? m : -INFINITY, l);
+}
+
+// Owner side (warps 0-7): one lane per row, each warp a group of 32 rows and a
+// range of 8-column chunks; O is staged as BF16 in 64-column, 128-byte
+// swizzled boxes of R rows and written by TMA stores (tmO has R-row boxes).
+template <int D>
+__device__ __forceinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t stage, int S, int w,
+                                          int warp, int lane, bool ok, const FwdParams& p,
+                                          const CUtensorMap* tmO, int bh, int q0) {
+  constexpr int kMaxS = 8;
+  constexpr int kC = D / 4;               // FP32 chunks per row
+  constexpr int kCB = D / 8;              // BF16 16-byte chunks per row
+  const int R = kBlockRows / S;
+  const int per_warp = (R / 32) * kCB / 8;   // BF16 chunks per warp (1 .. 8)
+  const int item0 = warp * per_warp;
+  const int lr = (item0 / kCB) * 32 + lane;
+  const int row = q0 + w * R + lr;
+  float ms[kMaxS], ls[kMaxS], wv[kMaxS];
+  float M = -INFINITY;
+#pragma unroll
+  for (int v = 0; v < kMaxS; ++v) {
+    ms[v] = -INFINITY;
+    ls[v] = 0.f;
+    if (v < S) {
+      const float2 ml = ld_shared_v2f(ml_base + (uint32_t)(v * R + lr) * 8u);
+      ms[v] = ml.x;
+      ls[v] = ml.y;
+      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+  }
+  float L = 0.f;
+#pragma unroll
+  for (int v = 0; v < kMaxS; ++v) {
+    wv[v] = ls[v] > 0.f ? ex2_approx(ms[v] - M) : 0.f;
+    L += wv[v] * ls[v];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int v = 0; v < kMaxS; ++v) wv[v] *= inv;
+  if ((item0 % kCB) == 0 && row < p.N_q && p.lse)
+    p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+#pragma unroll 1
+  for (int i = 0; i < per_warp; ++i) {
+    const int cb = (item0 + i) % kCB;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int v = 0; v < kMaxS; ++v) {
+      if (v < S) {
+        const uint32_t a = sb + (uint32_t)((v * kC + 2 * cb) * R + lr) * 16u;
+        const float4 t0 = ld_shared_v4f(a);
+        const float4 t1 = ld_shared_v4f(a + (uint32_t)R * 16u);
+        acc[0] += wv[v] * t0.x; acc[1] += wv[v] * t0.y; acc[2] += wv[v] * t0.z; acc[3] += wv[v] * t0.w;
+        acc[4] += wv[v] * t1.x; acc[5] += wv[v] * t1.y; acc[6] += wv[v] * t1.z; acc[7] += wv[v] * t1.w;
+      }
+    }
+    const int bx = cb >> 3, cbb = cb & 7;
+    st_shared_v4(stage + (uint32_t)(bx * R + lr) * 128u + ((uint32_t)(cbb ^ (lr & 7)) << 4),
+                 pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                 pack_bf16x2(acc[6], acc[7]));
+  }
+  fence_proxy_async_smem();
+  const bool all_ok = named_bar_and(1, 256, ok);
+  if (all_ok && warp == 0 && lane == 0 && q0 + w * R < p.N_q) {   // rows past N_q are clipped
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx)
+      tma_store_3d(tmO, stage + (uint32_t)(bx * R) * 128u, bx * 64, q0 + w * R, bh);
+    bulk_commit();
+    bulk_wait_read0();
+  }
+}
+
 // Query block and key-tile counts of work unit u (see the kernel's unit comment).
 struct UnitInfo {
   int bh, qb, split, S, slot, lo, n0, n1, nmax;
@@ -178,7 +297,8 @@ __device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int u) {
 template <int D, bool MC>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ CUtensorMap tmP, const FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -221,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- set-up
-  if (threadIdx.x == 0) {
+  // ---- set-up. The producer lane initialises the barriers and starts the Q
+  // loads at once, so they overlap the rest of the set-up.
+  if (warp == kWarpProducer && lane == 0) {
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarFull + s), 1);
@@ -236,18 +357,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kBarDrain), 1);
     *s_abort = 0;
     fence_mbar_init();
+    fence_proxy_async_smem();
     // the merge kernel (launched as a programmatic dependent) may be scheduled
     // once every CTA of this grid has started; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    // this grid may itself start before the previous kernel on the stream has
+    // finished (programmatic launch): no global read before this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (n_loop > 0) {
+      mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
+#pragma unroll
+      for (int X = 0; X < 2; ++X)
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sb + C::kOffQ + X * C::kTileBytes + bx * C::kBoxBytes, &tmQ, bar(C::kBarQ),
+                      bx * 64, q0 + X * kTileM, bh);
+    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
   }
   tc_fence_before();
   __syncthreads();
@@ -262,14 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpProducer) {
       // ======================= TMA producer =======================
       if (lane == 0 && n_loop > 0) {
-        int issued = 0;  // K/V tile loads issued
-        mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
-#pragma unroll
-        for (int X = 0; X < 2; ++X)
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(sb + C::kOffQ + X * C::kTileBytes + bx * C::kBoxBytes, &tmQ, bar(C::kBarQ),
-                        bx * 64, q0 + X * kTileM, bh);
+        int issued = 0;  // K/V tile loads issued (the Q loads were issued at set-up)
         const uint64_t pol = policy_evict_last();
         bool ok = true;
         for (int j = 0; j < n_loop && ok; ++j) {
@@ -401,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     // warps 10-11: idle members of warpgroup 2
+    if (p.cm) {   // the two cluster barriers of the in-cluster merge
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ======================= softmax warpgroups =======================
@@ -479,17 +608,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::kBarP + X));
       l += rs;
     }
-    if (ok && n > 0) {
+    // O_X is final once every MMA has completed; the Q tile and the K/V ring are
+    // then free and stage the outputs for coalesced TMA stores
+    if (ok && n_loop > 0) {
       ok = mbar_wait(bar(C::kBarO), 0, s_abort, p.status);
       tc_fence_after();
     }
+    // global writes only after the previous kernel on the stream has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool valid_row = row < p.N_q;
-    if (slot < 0) {
-      // ---- final epilogue: O / l -> BF16, LSE
+    if (p.cm) {
+      // every CTA of the cluster has finished its key range once all its
+      // threads pass the first cluster barrier: the Q tiles and the K/V ring
+      // are free and receive the partials (warpgroup 2 takes the same barriers)
+      cluster_sync();
+      cm_send<D>(sb + C::kOffQ, sb + C::kOffCm, p.s_tail, ui.split, X * kTileM + r, tO, n, m_ref, l);
+      cluster_sync();   // all partials of this CTA's rows have landed
+      cm_reduce<D>(sb + C::kOffQ, sb + C::kOffCm, sb + C::kOffQ + C::kCmStage, p.s_tail, ui.split, warp,
+                   lane, ok, p, &tmO, bh, q0);
+    } else if (slot < 0) {
+      // ---- final epilogue: O / l -> BF16 into this tile's Q slot (128-byte
+      // swizzled boxes, the tensor map's layout), then one TMA store; LSE direct
+      const uint32_t obase = sb + C::kOffQ + X * C::kTileBytes;
       if (ok) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow =
-            reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N_q + row) * D;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           float ov[32];
@@ -500,39 +642,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = 0.f;
           }
-          if (valid_row) {
+          const uint32_t rowaddr = obase + (uint32_t)(cc >> 6) * C::kBoxBytes + (uint32_t)r * 128u;
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-              st_global_v4(orow + cc + 8 * g, pack_bf16x2(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
-                           pack_bf16x2(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
-                           pack_bf16x2(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
-                           pack_bf16x2(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t ch = (uint32_t)(((cc & 63) >> 3) + g);   // 16-byte chunk in the row
+            st_shared_v4(rowaddr + ((ch ^ (uint32_t)(r & 7)) << 4),
+                         pack_bf16x2(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
+                         pack_bf16x2(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
+                         pack_bf16x2(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
+                         pack_bf16x2(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
           }
         }
         if (valid_row && p.lse)
           p.lse[(size_t)bh * p.N_q + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
-    } else if (ok) {
-      // ---- partial: unnormalised O and (m, l) of this key range to the workspace
-      const size_t prow = (size_t)slot * kBlockRows + X * kTileM + r;
-      float* po = p.part_o + prow * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
-        float ov[32];
-        if (n > 0) {
-          tmem_ld32(tO + cc, ov);
-          tmem_wait_ld();
-        } else {
+      fence_proxy_async_smem();
+      const bool all_ok = named_bar_and(1 + X, 128, ok);
+      if (all_ok && r == 0 && tile_first_row < p.N_q) {   // rows past N_q are clipped by the TMA
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          __stcg(reinterpret_cast<float4*>(po + cc) + g,
-                 make_float4(ov[4 * g], ov[4 * g + 1], ov[4 * g + 2], ov[4 * g + 3]));
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_store_3d(&tmO, obase + bx * C::kBoxBytes, bx * 64, tile_first_row, bh);
+        bulk_commit();
+        bulk_wait_read0();
       }
-      __stcg(reinterpret_cast<float2*>(p.part_ml) + prow,
-             make_float2(l > 0.f ? m_ref : -INFINITY, l));
+    } else {
+      // ---- partial: unnormalised O (FP32, 32-column swizzled boxes staged in the
+      // K/V ring, one TMA store) and (m, l) of this key range to the workspace
+      const uint32_t pbase = sb + C::kOffKV + X * 2 * C::kTileBytes;
+      const int prow0 = slot * kBlockRows + X * kTileM;
+      if (ok) {
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          float ov[32];
+          if (n > 0) {
+            tmem_ld32(tO + cc, ov);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+          }
+          const uint32_t rowaddr = pbase + (uint32_t)(cc >> 5) * C::kBoxBytes + (uint32_t)r * 128u;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            st_shared_v4(rowaddr + (((uint32_t)g ^ (uint32_t)(r & 7)) << 4), __float_as_uint(ov[4 * g]),
+                         __float_as_uint(ov[4 * g + 1]), __float_as_uint(ov[4 * g + 2]),
+                         __float_as_uint(ov[4 * g + 3]));
+        }
+        __stcg(reinterpret_cast<float2*>(p.part_ml) + prow0 + r,
+               make_float2(l > 0.f ? m_ref : -INFINITY, l));
+      }
+      fence_proxy_async_smem();
+      const bool all_ok = named_bar_and(1 + X, 128, ok);
+      if (all_ok && r == 0) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) tma_store_2d(&tmP, pbase + bx * C::kBoxBytes, bx * 32, prow0);
+        bulk_commit();
+        bulk_wait_read0();
+      }
     }
   }
 
@@ -628,41 +794,68 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   if (lane == 0 && p.lse) p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
+// Opt in to the kernel's dynamic shared memory (once per process and device set-up).
 template <int D, bool MC>
-cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const FwdParams& p, int units, cudaStream_t stream) {
+cudaError_t ensure_smem_attr() {
   static bool attr = false;  // benign race: setting the attribute twice is harmless
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  if (!MC) {
-    fa_fwd_kernel<D, false><<<units, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
-  }
+  if (attr) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<D>::kSmemBytes);
+  if (e == cudaSuccess) attr = true;
+  return e;
+}
+
+template <int D>
+int cluster_capacity_t(int s) {
+  if (ensure_smem_attr<D, false>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)((units + 1) & ~1));   // whole clusters of two
+  cfg.gridDim = dim3((unsigned)s);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
-  cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.x = (unsigned)s;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, true>, tq, tk, tv, p);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fa_fwd_kernel<D, false>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int D, bool MC>
+cudaError_t launch_main_t(const FwdMaps& m, const FwdParams& p, int units, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr<D, MC>();
+  if (e != cudaSuccess) return e;
+  // programmatic launch: set-up may overlap the previous kernel on the stream
+  // (the kernel waits for it before its first global read and write)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(MC ? ((units + 1) & ~1) : units));   // MC: whole clusters of two
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = MC ? 2 : (p.cm ? p.s_tail : 1);   // pairs, or the S splits of a block
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = (MC || p.cm) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, MC>, m.q, m.k, m.v, m.o, m.part, p);
 }
 
 template <int D>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, int units, bool multicast, cudaStream_t stream) {
-  cudaError_t e = multicast ? launch_main_t<D, true>(tq, tk, tv, p, units, stream)
-                            : launch_main_t<D, false>(tq, tk, tv, p, units, stream);
-  if (e != cudaSuccess || p.n_tail == 0) return e;
+cudaError_t launch_fwd_t(const FwdMaps& m, const FwdParams& p, int units, bool multicast,
+                         cudaStream_t stream) {
+  cudaError_t e = multicast ? launch_main_t<D, true>(m, p, units, stream)
+                            : launch_main_t<D, false>(m, p, units, stream);
+  if (e != cudaSuccess || p.n_tail == 0 || p.cm) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(((long long)p.n_tail * kBlockRows + 7) / 8));
   cfg.blockDim = dim3(256);
@@ -678,15 +871,25 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 }  // namespace
 
+int fwd_cluster_capacity(int d, int s) {
+  if (s < 2 || s > 8) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  static int cache[64][2][9];   // 0 = not yet asked, else capacity + 1
+  int& c = cache[dev][d == 128 ? 1 : 0][s];
+  if (c == 0) c = 1 + (d == 128 ? cluster_capacity_t<128>(s) : cluster_capacity_t<64>(s));
+  return c - 1;
+}
+
 size_t fwd_smem_bytes(int d) {
   return d == 128 ? (size_t)Cfg<128>::kSmemBytes : (size_t)Cfg<64>::kSmemBytes;
 }
 
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int units, bool multicast, cudaStream_t stream) {
+cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, bool multicast,
+                       cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  return d == 128 ? launch_fwd_t<128>(tq, tk, tv, p, units, multicast, stream)
-                  : launch_fwd_t<64>(tq, tk, tv, p, units, multicast, stream);
+  return d == 128 ? launch_fwd_t<128>(m, p, units, multicast, stream)
+                  : launch_fwd_t<64>(m, p, units, multicast, stream);
 }
 
 }  // namespace fa

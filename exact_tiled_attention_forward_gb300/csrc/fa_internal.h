@@ -24,6 +24,7 @@ struct FwdParams {
   int n_tail;       // query blocks u_full .. u_full+n_tail-1 are split ...
   int s_tail;       // ... into s_tail key ranges each (units u_full + t*s_tail + s)
   int n_units;      // work units (the grid may hold one more, idle, CTA to complete a cluster)
+  int cm;           // 1: every block is split and its s_tail CTAs (one cluster) merge in-kernel
   float c;          // scale * log2(e)
   void* o;          // bf16 [B][H_q][N_q][d]
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
@@ -36,9 +37,14 @@ struct FwdParams {
 struct FwdPlan {
   int u_full, n_tail, s_tail;
   long long units;      // CTAs of the fused kernel
-  size_t part_bytes;    // workspace for the split partials (0 when n_tail == 0)
+  size_t part_bytes;    // workspace for the split partials (0 without a merge kernel)
+  int cluster_merge;    // 1: all blocks split, partials merged inside each cluster of s_tail CTAs
 };
-FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms);
+// cluster_cap[s] (s = 2..8): clusters of s CTAs the device holds at once, 0 if
+// unusable; nullptr disables the in-cluster merge.
+FwdPlan plan_forward(long long blocks, int kv_tiles, bool causal, int d, int sms, const int* cluster_cap);
+// Clusters of s fused-kernel CTAs (head dim d) resident at once on the current device.
+int fwd_cluster_capacity(int d, int s);
 
 // Shared-memory bytes the fused kernel needs for head dim d (64 or 128).
 size_t fwd_smem_bytes(int d);
@@ -47,8 +53,13 @@ size_t fwd_smem_bytes(int d);
 // kernel as its programmatic dependent on the same stream. With multicast,
 // CTAs run in clusters of two that share K/V tile loads (no split plans;
 // tk / tv must then be built with 64-row boxes).
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int units, bool multicast, cudaStream_t stream);
+// Tensor maps of one forward call: Q, K, V, O (BF16, [B*H][N][d], 64-column
+// boxes, 128-byte swizzle) and the FP32 split partials ([rows][d], 32-column boxes).
+struct FwdMaps {
+  CUtensorMap q, k, v, o, part;
+};
+cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, bool multicast,
+                       cudaStream_t stream);
 
 // ---- decode / few queries per KV head -------------------------------------------------
 constexpr int kDecodeMaxRows = 16;   // R = G * N_q rows per KV head must fit one m16 MMA
@@ -111,6 +122,9 @@ extern thread_local int g_last_cuda_error;
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);
+
+// 2-D FP32 tensor map over [rows][inner] with a {32, 128} box, 128-byte swizzle.
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows);
 
 int* device_status_ptr();   // address of the current device's status word (nullptr on error)
 

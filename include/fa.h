@@ -59,8 +59,14 @@ typedef enum {
 /* Exact attention forward, fused (the tiled online-softmax kernel).
  * Prefill: tcgen05/TMA kernel, two 128-row query tiles per CTA, K/V tiles of
  * 128 keys. Query blocks that do not fill a whole wave of the GPU have their
- * key range split over several CTAs; a second kernel (programmatic dependent
- * launch on the same stream) merges the partial (m, l, O) results.
+ * key range split over several CTAs. When every block is split (fewer blocks
+ * than SMs), the CTAs of a block run as one thread-block cluster and merge
+ * their partial (m, l, O) results through distributed shared memory at the
+ * end of the kernel (no workspace, one launch); otherwise a second kernel
+ * (programmatic dependent launch on the same stream) merges them. The main
+ * kernel is itself a programmatic dependent launch: its set-up may overlap the
+ * previous kernel on the stream, and it reads and writes global memory only
+ * after that kernel has completed.
  * Decode / few queries (the H_q/H_kv * N_q query rows that share a KV head
  * number at most 16): one CTA per (batch, KV head, 128-key chunk) reads its
  * K and V chunk once for all those rows; chunk partials are merged the same way.
@@ -110,6 +116,21 @@ int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float
 
 /* Bytes of workspace fa_naive_forward needs: B*H_q*N_q*roundup(N_k, 8)*2. 0 on bad sizes. */
 size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k);
+
+/* How fa_forward would run a request on the current device, without running
+ * it (no paper counterpart: a planning query for callers that size buffers or
+ * count launches). Same shape checks as fa_forward (no pointers involved).
+ * Outputs (each may be NULL): *ctas = CTAs of the main kernel; *launches =
+ * kernels one call enqueues (0 for an empty request, 1, or 2 when a merge
+ * kernel follows); *workspace_bytes = stream-ordered workspace the call
+ * allocates, which is also the scratch fa_forward_noalloc needs (0 when the
+ * split partials are merged inside thread-block clusters). The plan depends on
+ * the device's SM count and cluster capacity, and on the environment switches
+ * FA_CLUSTER_MERGE=0 (merge kernel instead of in-cluster merge) and
+ * FA_MULTICAST=1 (paired K/V loads). Returns FA_OK, FA_ERR_INVALID_ARG or
+ * FA_ERR_UNSUPPORTED. */
+int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal, long long* ctas,
+                    int* launches, size_t* workspace_bytes);
 
 /* Static description of an fa_status code. Never NULL. */
 const char* fa_status_string(int status);

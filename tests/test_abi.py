@@ -26,7 +26,7 @@ def lib():
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
     assert set(names) == {"fa_forward", "fa_forward_noalloc", "fa_naive_forward",
-                          "fa_naive_workspace_bytes",
+                          "fa_naive_workspace_bytes", "fa_forward_plan",
                           "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
                           "fa_version"}
     for n in names:

@@ -71,6 +71,34 @@ def test_small_shapes(fa, shape):
     compare(o, lse, *run_oracle(a))
 
 
+# Split plans: every query block's key range is cut over several CTAs. The
+# partials are merged either inside a thread-block cluster (default when every
+# block is split) or by the merge kernel (FA_CLUSTER_MERGE=0); both against the oracle.
+SPLIT = [
+    (1, 1, 1, 8192, 8192, 128, False),   # 32 blocks x 4 key ranges (the one-head workload)
+    (1, 1, 1, 2000, 3000, 64, False),    # ragged, d = 64, eight key ranges
+    (2, 3, 1, 700, 1500, 128, True),     # causal, GQA, unequal ranges inside a cluster
+    (1, 1, 1, 256, 2048, 128, False),    # a single block
+]
+
+
+@pytest.mark.parametrize("cluster_merge", [True, False], ids=["cluster", "kernel"])
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s[:6])) + ("c" if s[6] else ""))
+def test_split_merge_modes(fa, shape, cluster_merge, monkeypatch):
+    monkeypatch.setenv("FA_CLUSTER_MERGE", "1" if cluster_merge else "0")
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=5, k_row_frac=0.01)
+    plan = fa.fa_forward_plan(B, Hq, Hkv, Nq, Nk, d, causal)
+    blocks = B * Hq * ((Nq + 255) // 256)
+    assert plan["ctas"] > blocks                     # the key ranges are split
+    if cluster_merge:
+        assert plan["launches"] == 1 and plan["workspace_bytes"] == 0
+    else:
+        assert plan["launches"] == 2 and plan["workspace_bytes"] > 0
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
 def test_tiny_workload_n256_d64(fa):
     a = I.make_workload("tiny_n256_d64")
     o, lse = _run(fa, a)

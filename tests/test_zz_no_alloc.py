@@ -45,38 +45,27 @@ def _call(fa, entry, q, k, v, o, lse, a):
     return st
 
 
-def _planned_scratch(a, sms):
-    """Scratch bytes of the split partials the planner picks (mirrors plan_forward in libfa)."""
-    n_qb = (a.N_q + 255) // 256
-    n_kv = (a.N_k + 127) // 128
-    kv_eff = (n_kv + 1) // 2 if a.causal else n_kv
-    blocks = a.B * a.H_q * n_qb
-    if blocks <= 0 or kv_eff <= 1:
-        return 0
-    tail = blocks if blocks < sms else (0 if a.causal else blocks % sms)
-    if tail == 0:
-        return 0
-    best, best_cost = 1, 1e30
-    for s in range(1, min(16, kv_eff) + 1):
-        waves = (tail * s + sms - 1) // sms
-        cost = waves * (2.0 + kv_eff / s) + (0.5 if s > 1 else 0.0)
-        if cost < best_cost - 1e-9:
-            best, best_cost = s, cost
-    if best == 1:
-        return 0
-    return tail * best * 256 * (a.d * 4 + 8)
+def _planned_scratch(fa, a):
+    """Scratch bytes of the split partials (the library's own plan for this request)."""
+    return fa.fa_forward_plan(a.B, a.H_q, a.H_kv, a.N_q, a.N_k, a.d, a.causal)["workspace_bytes"]
 
 
-@pytest.mark.parametrize("shape", [
-    (1, 1, 1, 8192, 8192, 128, False),   # one head, N = 8192: split over 4 CTAs per block
-    (1, 2, 1, 700, 3000, 64, True),      # causal, GQA, ragged, d = 64
+@pytest.mark.parametrize("shape,cluster_merge", [
+    # split partials through the scratch array (merge kernel)
+    ((1, 1, 1, 8192, 8192, 128, False), False),   # one head, N = 8192: split over 4 CTAs per block
+    ((1, 2, 1, 700, 3000, 64, True), False),      # causal, GQA, ragged, d = 64
+    # split partials merged inside clusters: no scratch at all
+    ((1, 1, 1, 8192, 8192, 128, False), True),
 ])
-def test_noalloc_matches_fa_forward_twice(fa, shape):
+def test_noalloc_matches_fa_forward_twice(fa, shape, cluster_merge, monkeypatch):
     import torch
+    monkeypatch.setenv("FA_CLUSTER_MERGE", "1" if cluster_merge else "0")
     a = I.make_inputs(*shape[:6], causal=shape[6], seed=3, k_row_frac=0.01)
     q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert 0 < _planned_scratch(a, sms) <= SCRATCH_BYTES   # the scratch path is exercised
+    if cluster_merge:
+        assert _planned_scratch(fa, a) == 0
+    else:
+        assert 0 < _planned_scratch(fa, a) <= SCRATCH_BYTES   # the scratch path is exercised
     o_ref = torch.empty((a.B, a.H_q, a.N_q, a.d), dtype=torch.bfloat16, device="cuda")
     l_ref = torch.empty((a.B, a.H_q, a.N_q), dtype=torch.float32, device="cuda")
     assert _call(fa, "fa_forward", q, k, v, o_ref, l_ref, a) == fa.FA_OK
@@ -99,13 +88,13 @@ def test_noalloc_matches_fa_forward_twice(fa, shape):
         assert np.abs(got_l[fin] - ref_l[fin]).max() <= TOL_MAX_ABS_LSE
 
 
-def test_noalloc_rejects_requests_beyond_scratch(fa):
+def test_noalloc_rejects_requests_beyond_scratch(fa, monkeypatch):
     import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    monkeypatch.setenv("FA_CLUSTER_MERGE", "0")   # partials through the scratch array
     # find a shape whose planned split partials exceed the fixed array
     for heads in range(40, 160, 4):
         a = I.make_inputs(1, heads, heads, 256, 4096, 128, seed=0)
-        if _planned_scratch(a, sms) > SCRATCH_BYTES:
+        if _planned_scratch(fa, a) > SCRATCH_BYTES:
             break
     else:
         pytest.skip("no candidate shape exceeds the scratch on this GPU")
