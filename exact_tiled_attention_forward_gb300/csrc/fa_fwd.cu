@@ -445,11 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kWarpMma) {
       // ======================= tcgen05 MMA issuer =======================
-      if (lane == 0 && n_loop > 0) {
+      // the whole warp runs this loop converged; elected lanes issue (see mma_ss_lh_w)
+      if (n_loop > 0) {
         // a stage is released to this CTA's producer, and with sharing to the partner's too
         auto release = [&](int st) {
-          if (share) mma_commit_mc(bar(C::kBarEmpty + st), (uint16_t)0x3);
-          else mma_commit(bar(C::kBarEmpty + st));
+          if (share) mma_commit_mc_w(bar(C::kBarEmpty + st), (uint16_t)0x3);
+          else mma_commit_w(bar(C::kBarEmpty + st));
         };
         constexpr uint32_t idS = idesc_bf16_f32(128, kTileN, false);
         constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk) {
             constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
             const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-            mma_ss_lh(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
+            mma_ss_lh_w(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
           }
         };
         auto issue_PV = [&](int X, int st, bool acc) {
@@ -478,15 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a = tmem + C::tm_s(X);
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 16kk .. 16kk+15 in columns 8kk ..
-            mma_ts_lh(d, a + (uint32_t)kk * 8u,
+            mma_ts_lh_w(d, a + (uint32_t)kk * 8u,
                       b0 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO, (acc || kk > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait(bar(C::kBarQ), 0, s_abort, p.status);
-        if (ok) ok = mbar_wait(bar(C::kBarFull + 0), 0, s_abort, p.status);
+        bool ok = mbar_wait_w(bar(C::kBarQ), 0, s_abort, p.status);
+        if (ok) ok = mbar_wait_w(bar(C::kBarFull + 0), 0, s_abort, p.status);
         if (ok) {
           tc_fence_after();
-          if (n0 > 0) { issue_S(0, 0); mma_commit(bar(C::kBarS + 0)); }
-          if (n1 > 0) { issue_S(1, 0); mma_commit(bar(C::kBarS + 1)); }
+          if (n0 > 0) { issue_S(0, 0); mma_commit_w(bar(C::kBarS + 0)); }
+          if (n1 > 0) { issue_S(1, 0); mma_commit_w(bar(C::kBarS + 1)); }
           release(0);
         }
         for (int j = 0; j < n_loop && ok; ++j) {
@@ -495,32 +496,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t phV = (uint32_t)(itV / C::kStages) & 1u;
           const uint32_t phK = (uint32_t)(itK / C::kStages) & 1u;
           const bool next = (j + 1) < n_loop;
-          if (!(ok = mbar_wait(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
+          if (!(ok = mbar_wait_w(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
           tc_fence_after();
           if (j < n0) {
-            if (!(ok = mbar_wait(bar(C::kBarP + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
+            if (!(ok = mbar_wait_w(bar(C::kBarP + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
             tc_fence_after();
             issue_PV(0, stV, j > 0);
           }
           if (next) {
-            if (!(ok = mbar_wait(bar(C::kBarFull + stK), phK, s_abort, p.status))) break;
+            if (!(ok = mbar_wait_w(bar(C::kBarFull + stK), phK, s_abort, p.status))) break;
             tc_fence_after();
-            if (j + 1 < n0) { issue_S(0, stK); mma_commit(bar(C::kBarS + 0)); }
+            if (j + 1 < n0) { issue_S(0, stK); mma_commit_w(bar(C::kBarS + 0)); }
           }
           if (j < n1) {
-            if (!(ok = mbar_wait(bar(C::kBarP + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
+            if (!(ok = mbar_wait_w(bar(C::kBarP + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
             tc_fence_after();
             issue_PV(1, stV, j > 0);
           }
           release(stV);
           if (next) {
-            if (j + 1 < n1) { issue_S(1, stK); mma_commit(bar(C::kBarS + 1)); }
+            if (j + 1 < n1) { issue_S(1, stK); mma_commit_w(bar(C::kBarS + 1)); }
             release(stK);
           }
         }
-        mma_commit(bar(C::kBarO));
+        mma_commit_w(bar(C::kBarO));
         // drain: all MMAs done before tensor memory is released
-        mma_commit(bar(C::kBarDrain));
+        mma_commit_w(bar(C::kBarDrain));
         drain_wait(bar(C::kBarDrain), 0, p.status);
       }
       __syncwarp();
