@@ -27,15 +27,20 @@
 // (all 128 scores of a row are in registers first) and is the A operand of the
 // PV MMA straight from tensor memory.
 // MMA issue order per key tile j (ping-pong between the two query tiles):
-//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-// The commit that signals S_X(j+1) also covers PV_X(j): when a softmax warp
-// sees S_X(j+1) the accumulator O_X is stable and may be rescaled in place.
+//   PV_A(j) keys 0..63, PV_A(j) keys 64..127, S_A(j+1), then the same for B
+// The softmax hands P over in two halves (keys 0..63, then 64..127), so the
+// first half of PV_X(j) runs while the second half of P is computed. The
+// commit that signals S_X(j+1) also covers PV_X(j): when a softmax warp sees
+// S_X(j+1) the accumulator O_X is stable and may be rescaled in place.
 //
-// Softmax per tile: exponentials are computed against the row's reference max
-// while the tile max is found alongside; only if a row's max rose by more
-// than 2^8 (log2 units) — always on its first live tile — is the tile redone
-// with the new reference and O, l rescaled. Until then P <= 2^8, exact in the final O / l
-// because O and l share the same stale reference.
+// Softmax per tile: exponentials are computed against the row's reference
+// max m (log2 units). A row's reference is set from the tile max on its first
+// live tile; afterwards P = 2^(s c - m) may exceed 1, and only when the first
+// half's sum of P exceeds 2^16 (so some P may) or the second half's max exceeds
+// m + 16 is the reference raised to the tile max, O and l rescaled and the
+// first half redone, all before P is handed over. P <= 2^16 keeps every value
+// in range, and the final O / l and LSE are exact because O and l share the
+// reference. An overflowed P makes the sum infinite and takes the same path.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -50,7 +55,8 @@ constexpr int kRegsSoftmax = 224;   // per thread, warpgroups 0-1
 constexpr int kRegsOther = 56;      // per thread, warpgroup 2
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
-constexpr float kTau = 8.0f;
+constexpr float kTau = 16.0f;          // a reference may lag the row max by this much (log2)
+constexpr float kSumCap = 65536.0f;    // 2^kTau
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -66,11 +72,12 @@ struct Cfg {
   static constexpr int kBarQ = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
-  static constexpr int kBarS = 1 + 2 * kStages;      // [2]
-  static constexpr int kBarP = 3 + 2 * kStages;      // [2]
-  static constexpr int kBarO = 5 + 2 * kStages;
-  static constexpr int kBarDrain = 6 + 2 * kStages;
-  static constexpr int kNumBars = 7 + 2 * kStages;
+  static constexpr int kBarS = 1 + 2 * kStages;      // [2] S_X ready
+  static constexpr int kBarP1 = 3 + 2 * kStages;     // [2] P_X keys 0..63 in TMEM
+  static constexpr int kBarP2 = 5 + 2 * kStages;     // [2] P_X keys 64..127 in TMEM
+  static constexpr int kBarO = 7 + 2 * kStages;
+  static constexpr int kBarDrain = 8 + 2 * kStages;
+  static constexpr int kNumBars = 9 + 2 * kStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // in-cluster merge: (m, l) of up to kCmRows partial rows received from the
   // cluster; their O rows land in [0, kOffBar) (the Q tiles and the K/V ring)
@@ -88,43 +95,76 @@ struct Cfg {
 __device__ __forceinline__ int min_i(int a, int b) { return a < b ? a : b; }
 __device__ __forceinline__ int max_i(int a, int b) { return a > b ? a : b; }
 
-// P = 2^(s*c - mb) for the 128 scores of this thread's row (FP32 pairs, one
-// packed FMA per pair), packed to BF16 and stored over the first 64 columns
-// of the row's S tile in TMEM. Returns the row sum of P (FP32); if mx is not
-// null it also returns the max of the raw scores.
-__device__ __forceinline__ float exp_tile(const float* s, float c, float mb, uint32_t tS, float* mx) {
-  float2 sa = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
-  float m0 = -INFINITY, m1 = -INFINITY;
+// P = 2^(s*c - mb) for 64 scores of this thread's row (FP32 pairs, one packed
+// FMA per pair), packed to BF16 and stored to 32 TMEM columns from tP. Returns
+// the sum of P (FP32). Software-pipelined in chunks of 16: the exponentials of
+// chunk k+1 are issued before chunk k is packed and stored, so the exp unit
+// stays busy.
+__device__ __forceinline__ float exp_half(const float* s, float c, float mb, uint32_t tP) {
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+  float pa[16], pb[16];
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    // the 32 exponentials of this chunk first (independent: the exp unit stays busy)
-    float pv[32];
+  for (int i = 0; i < 16; i += 2) {
+    const float2 e = ffma2_bc(make_float2(s[i], s[i + 1]), c, -mb);
+    pa[i] = ex2_approx(e.x);
+    pa[i + 1] = ex2_approx(e.y);
+  }
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const float2 e = ffma2_bc(make_float2(s[cc * 32 + i], s[cc * 32 + i + 1]), c, -mb);
-      pv[i] = ex2_approx(e.x);
-      pv[i + 1] = ex2_approx(e.y);
-    }
-    // then BF16 packing and the TMEM store, row sums, running max of the raw scores
-    uint32_t pk[16];
+  for (int k = 0; k < 4; ++k) {
+    if (k + 1 < 4) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
-    tmem_st16(tS + cc * 16, pk);
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      sa = fadd2(sa, make_float2(pv[i], pv[i + 1]));
-      sb2 = fadd2(sb2, make_float2(pv[i + 2], pv[i + 3]));
-    }
-    if (mx) {
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        m0 = max3f(m0, s[cc * 32 + i], s[cc * 32 + i + 1]);
-        m1 = max3f(m1, s[cc * 32 + i + 2], s[cc * 32 + i + 3]);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 e = ffma2_bc(make_float2(s[(k + 1) * 16 + i], s[(k + 1) * 16 + i + 1]), c, -mb);
+        pb[i] = ex2_approx(e.x);
+        pb[i + 1] = ex2_approx(e.y);
       }
     }
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(pa[2 * i], pa[2 * i + 1]);
+    tmem_st8(tP + (uint32_t)k * 8u, pk);
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      sa = fadd2(sa, make_float2(pa[i], pa[i + 1]));
+      sb = fadd2(sb, make_float2(pa[i + 2], pa[i + 3]));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pa[i] = pb[i];
   }
-  if (mx) *mx = fmaxf(m0, m1);
-  return (sa.x + sa.y) + (sb2.x + sb2.y);
+  return (sa.x + sa.y) + (sb.x + sb.y);
+}
+
+// Max of n (a multiple of 4) raw scores.
+template <int N>
+__device__ __forceinline__ float max_scores(const float* s) {
+  float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    a0 = max3f(a0, s[i], s[i + 1]);
+    a1 = max3f(a1, s[i + 2], s[i + 3]);
+  }
+  return fmaxf(a0, a1);
+}
+
+// O_X *= alpha for this thread's row (all lanes of the warp take part).
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    float ov[32];
+    tmem_ld32(tO + cc, ov);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+    tmem_st32(tO + cc, ov);
+  }
+}
+
+// Hand P (or half of it) to the MMA warp: stores complete, then arrive.
+__device__ __forceinline__ void publish(uint32_t bar) {
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(bar);
 }
 
 // Bounded wait used on drain paths: ignores the abort flag, still gives up after the timeout.
@@ -351,8 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::kBarS + 0), 1);
     mbar_init(bar(C::kBarS + 1), 1);
-    mbar_init(bar(C::kBarP + 0), 128);   // all 128 rows of the tile
-    mbar_init(bar(C::kBarP + 1), 128);
+    for (int X = 0; X < 2; ++X) {
+      mbar_init(bar(C::kBarP1 + X), 128);   // all 128 rows of the tile
+      mbar_init(bar(C::kBarP2 + X), 128);
+    }
     mbar_init(bar(C::kBarO), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *s_abort = 0;
@@ -473,12 +515,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_lh_w(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_PV = [&](int X, int st, bool acc) {
+        auto issue_PV = [&](int X, int st, bool acc, int h) {   // keys 64h .. 64h+63
           const uint32_t b0 = lv0 + (uint32_t)st * kStageStep;
           const uint32_t d = tmem + C::tm_o(X);
           const uint32_t a = tmem + C::tm_s(X);
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 16kk .. 16kk+15 in columns 8kk ..
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // P of keys 16kk .. 16kk+15 in columns 8kk ..
             mma_ts_lh_w(d, a + (uint32_t)kk * 8u,
                       b0 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO, (acc || kk > 0) ? 1u : 0u);
         };
@@ -499,9 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait_w(bar(C::kBarFull + stV), phV, s_abort, p.status))) break;
           tc_fence_after();
           if (j < n0) {
-            if (!(ok = mbar_wait_w(bar(C::kBarP + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
+            if (!(ok = mbar_wait_w(bar(C::kBarP1 + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
             tc_fence_after();
-            issue_PV(0, stV, j > 0);
+            issue_PV(0, stV, j > 0, 0);
+            if (!(ok = mbar_wait_w(bar(C::kBarP2 + 0), (uint32_t)j & 1u, s_abort, p.status))) break;
+            tc_fence_after();
+            issue_PV(0, stV, true, 1);
           }
           if (next) {
             if (!(ok = mbar_wait_w(bar(C::kBarFull + stK), phK, s_abort, p.status))) break;
@@ -509,9 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 1 < n0) { issue_S(0, stK); mma_commit_w(bar(C::kBarS + 0)); }
           }
           if (j < n1) {
-            if (!(ok = mbar_wait_w(bar(C::kBarP + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
+            if (!(ok = mbar_wait_w(bar(C::kBarP1 + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
             tc_fence_after();
-            issue_PV(1, stV, j > 0);
+            issue_PV(1, stV, j > 0, 0);
+            if (!(ok = mbar_wait_w(bar(C::kBarP2 + 1), (uint32_t)j & 1u, s_abort, p.status))) break;
+            tc_fence_after();
+            issue_PV(1, stV, true, 1);
           }
           release(stV);
           if (next) {
@@ -568,49 +616,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // warp-uniform: every row of the warp has a reference max
       const bool spec = !__any_sync(0xffffffffu, m_ref == -INFINITY);
-      float rs = 0.f, mx;
-      if (spec) {
-        rs = exp_tile(s, c, m_ref, tS, &mx);
-      } else {
-        float a0 = s[0], a1 = s[1];
-#pragma unroll
-        for (int i = 2; i < kTileN - 2; i += 4) {
-          a0 = max3f(a0, s[i], s[i + 1]);
-          a1 = max3f(a1, s[i + 2], s[i + 3]);
-        }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(s[kTileN - 2], s[kTileN - 1]));
-      }
-      const float m_tile = mx * c;
-      const bool need = m_tile > m_ref + kTau;   // always true on a row's first live tile
-      const bool any_need = __any_sync(0xffffffffu, need);
-      if (any_need) {
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2_approx(m_ref - m_tile);  // 0 when the row had no reference yet
-          m_ref = m_tile;
-          l *= alpha;
-        }
-        if (j > 0) {
-          // O_X holds PV_X(0..j-1) and is stable (covered by the S_X(j) commit)
-#pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            float ov[32];
-            tmem_ld32(tO + cc, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-            tmem_st32(tO + cc, ov);
+      if (!spec) {
+        // some row's first live tile: references from the tile max
+        const float m_tile = max_scores<kTileN>(s) * c;
+        const bool need = m_tile > m_ref + kTau;   // always, for a row without a reference
+        if (__any_sync(0xffffffffu, need)) {
+          float alpha = 1.f;
+          if (need) {
+            alpha = ex2_approx(m_ref - m_tile);  // 0 when the row had no reference yet
+            m_ref = m_tile;
+            l *= alpha;
           }
+          if (j > 0) rescale_o<D>(tO, alpha);   // O_X holds PV_X(0..j-1), stable (S_X(j) commit)
         }
+        const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+        const float r1 = exp_half(s, c, mb, tS);
+        publish(bar(C::kBarP1 + X));
+        const float r2 = exp_half(s + 64, c, mb, tS + 32);
+        publish(bar(C::kBarP2 + X));
+        l += r1 + r2;
+      } else {
+        // the first half's P against the reference, and the second half's max:
+        // any rescale is decided here, while O_X is stable (S_X(j) commit)
+        float r1 = exp_half(s, c, m_ref, tS);
+        const float m2 = max_scores<kTileN / 2>(s + 64) * c;
+        const bool need = !(r1 <= kSumCap) || m2 > m_ref + kTau;
+        if (__any_sync(0xffffffffu, need)) {
+          float alpha = 1.f;
+          if (need) {
+            const float m_new = fmaxf(m_ref, fmaxf(max_scores<kTileN / 2>(s) * c, m2));
+            alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+            l *= alpha;
+          }
+          rescale_o<D>(tO, alpha);
+          r1 = exp_half(s, c, m_ref, tS);
+        }
+        publish(bar(C::kBarP1 + X));
+        // the second half's P <= 2^kTau now
+        const float r2 = exp_half(s + 64, c, m_ref, tS + 32);
+        publish(bar(C::kBarP2 + X));
+        l += r1 + r2;
       }
-      if (any_need || !spec) rs = exp_tile(s, c, m_ref == -INFINITY ? 0.f : m_ref, tS, nullptr);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarP + X));
-      l += rs;
     }
-    // O_X is final once every MMA has completed; the Q tile and the K/V ring are
-    // then free and stage the outputs for coalesced TMA stores
     if (ok && n_loop > 0) {
       ok = mbar_wait(bar(C::kBarO), 0, s_abort, p.status);
       tc_fence_after();
