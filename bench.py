@@ -40,9 +40,14 @@ METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofli
 DEFAULT_WORKLOAD = "one_head_n8192_d128"
 DECODE_WORKLOAD = "decode_b16_h32_kv8_n8192_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
-                  "exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
-                  "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"]
+# the sources each profiled kernel is built from (a summary's traffic figure is
+# used only while their hash matches the one recorded with it)
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
+                      "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
+    "fa_decode_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
+                         "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
+}
 
 
 def load_peaks():
@@ -54,9 +59,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -71,7 +76,7 @@ def profiled_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
     text = open(path).read()
     m_b = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
     m_h = re.search(r"^kernel_source_sha256_16:\s*([0-9a-f]+)", text, re.M)
-    if not m_b or not m_h or m_h.group(1) != kernel_hash():
+    if not m_b or not m_h or m_h.group(1) != kernel_hash(kernel):
         return None
     return float(m_b.group(1))
 
