@@ -217,64 +217,74 @@ __device__ __forceinline__ void cm_send(uint32_t sb, uint32_t ml_base, int S, in
 }
 
 // Owner side (warps 0-7): one lane per row, each warp a group of 32 rows and a
-// range of 8-column chunks; O is staged as BF16 in 64-column, 128-byte
-// swizzled boxes of R rows and written by TMA stores (tmO has R-row boxes).
-template <int D>
-__device__ __forceinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t stage, int S, int w,
-                                          int warp, int lane, bool ok, const FwdParams& p,
-                                          const CUtensorMap* tmO, int bh, int q0) {
-  constexpr int kMaxS = 8;
+// range of 8-column chunks, two chunks at a time with all their loads issued
+// first; O is staged as BF16 in 64-column, 128-byte swizzled boxes of R rows and
+// written by TMA stores (tmO has R-row boxes). S (2, 4 or 8) is a template
+// parameter so the per-source arrays are exactly sized. Not inlined: it runs
+// once per CTA, and compiled apart it leaves the main loop's registers alone.
+template <int D, int S>
+__device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t stage, int w, int warp,
+                                       int lane, bool ok, const FwdParams& p, const CUtensorMap* tmO,
+                                       int bh, int q0) {
   constexpr int kC = D / 4;               // FP32 chunks per row
   constexpr int kCB = D / 8;              // BF16 16-byte chunks per row
-  const int R = kBlockRows / S;
-  const int per_warp = (R / 32) * kCB / 8;   // BF16 chunks per warp (1 .. 8)
-  const int item0 = warp * per_warp;
+  constexpr int R = kBlockRows / S;
+  constexpr int kPerWarp = (R / 32) * kCB / 8;   // BF16 chunks per warp (1 .. 8)
+  const int item0 = warp * kPerWarp;
   const int lr = (item0 / kCB) * 32 + lane;
   const int row = q0 + w * R + lr;
-  float ms[kMaxS], ls[kMaxS], wv[kMaxS];
+  float ms[S], ls[S], wv[S];
   float M = -INFINITY;
 #pragma unroll
-  for (int v = 0; v < kMaxS; ++v) {
-    ms[v] = -INFINITY;
-    ls[v] = 0.f;
-    if (v < S) {
-      const float2 ml = ld_shared_v2f(ml_base + (uint32_t)(v * R + lr) * 8u);
-      ms[v] = ml.x;
-      ls[v] = ml.y;
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
+  for (int v = 0; v < S; ++v) {
+    const float2 ml = ld_shared_v2f(ml_base + (uint32_t)(v * R + lr) * 8u);
+    ms[v] = ml.x;
+    ls[v] = ml.y;
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
   }
   float L = 0.f;
 #pragma unroll
-  for (int v = 0; v < kMaxS; ++v) {
+  for (int v = 0; v < S; ++v) {
     wv[v] = ls[v] > 0.f ? ex2_approx(ms[v] - M) : 0.f;
     L += wv[v] * ls[v];
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int v = 0; v < kMaxS; ++v) wv[v] *= inv;
+  for (int v = 0; v < S; ++v) wv[v] *= inv;
   if ((item0 % kCB) == 0 && row < p.N_q && p.lse)
     p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+  constexpr int kStep = kPerWarp >= 2 ? 2 : 1;
 #pragma unroll 1
-  for (int i = 0; i < per_warp; ++i) {
-    const int cb = (item0 + i) % kCB;
-    float acc[8];
+  for (int i = 0; i < kPerWarp; i += kStep) {
+    float4 t[kStep][S][2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    for (int q = 0; q < kStep; ++q) {
+      const int cb = (item0 + i + q) % kCB;
 #pragma unroll
-    for (int v = 0; v < kMaxS; ++v) {
-      if (v < S) {
+      for (int v = 0; v < S; ++v) {
         const uint32_t a = sb + (uint32_t)((v * kC + 2 * cb) * R + lr) * 16u;
-        const float4 t0 = ld_shared_v4f(a);
-        const float4 t1 = ld_shared_v4f(a + (uint32_t)R * 16u);
-        acc[0] += wv[v] * t0.x; acc[1] += wv[v] * t0.y; acc[2] += wv[v] * t0.z; acc[3] += wv[v] * t0.w;
-        acc[4] += wv[v] * t1.x; acc[5] += wv[v] * t1.y; acc[6] += wv[v] * t1.z; acc[7] += wv[v] * t1.w;
+        t[q][v][0] = ld_shared_v4f(a);
+        t[q][v][1] = ld_shared_v4f(a + (uint32_t)R * 16u);
       }
     }
-    const int bx = cb >> 3, cbb = cb & 7;
-    st_shared_v4(stage + (uint32_t)(bx * R + lr) * 128u + ((uint32_t)(cbb ^ (lr & 7)) << 4),
-                 pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                 pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int q = 0; q < kStep; ++q) {
+      const int cb = (item0 + i + q) % kCB;
+      float acc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+      for (int v = 0; v < S; ++v) {
+        acc[0] += wv[v] * t[q][v][0].x; acc[1] += wv[v] * t[q][v][0].y;
+        acc[2] += wv[v] * t[q][v][0].z; acc[3] += wv[v] * t[q][v][0].w;
+        acc[4] += wv[v] * t[q][v][1].x; acc[5] += wv[v] * t[q][v][1].y;
+        acc[6] += wv[v] * t[q][v][1].z; acc[7] += wv[v] * t[q][v][1].w;
+      }
+      const int bx = cb >> 3, cbb = cb & 7;
+      st_shared_v4(stage + (uint32_t)(bx * R + lr) * 128u + ((uint32_t)(cbb ^ (lr & 7)) << 4),
+                   pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+    }
   }
   fence_proxy_async_smem();
   const bool all_ok = named_bar_and(1, 256, ok);
@@ -674,8 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       cluster_sync();
       cm_send<D>(sb + C::kOffQ, sb + C::kOffCm, p.s_tail, ui.split, X * kTileM + r, tO, n, m_ref, l);
       cluster_sync();   // all partials of this CTA's rows have landed
-      cm_reduce<D>(sb + C::kOffQ, sb + C::kOffCm, sb + C::kOffQ + C::kCmStage, p.s_tail, ui.split, warp,
-                   lane, ok, p, &tmO, bh, q0);
+      {
+        const uint32_t rb = sb + C::kOffQ, mb2 = sb + C::kOffCm, stg = sb + C::kOffQ + C::kCmStage;
+        if (p.s_tail == 2) cm_reduce<D, 2>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        else if (p.s_tail == 4) cm_reduce<D, 4>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        else cm_reduce<D, 8>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+      }
     } else if (slot < 0) {
       // ---- final epilogue: O / l -> BF16 into this tile's Q slot (128-byte
       // swizzled boxes, the tensor map's layout), then one TMA store; LSE direct
