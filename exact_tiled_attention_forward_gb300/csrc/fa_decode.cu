@@ -5,19 +5,22 @@
 // generating one token at a time?": split the key sequence across thread
 // blocks and combine).
 //
-// Work unit = (batch, KV head, chunk of 128 keys). The rows of a unit are all
-// query rows that read this KV head: R = G * N_q <= 16 (G = H_q / H_kv, GQA),
-// which is exactly the M = 16 of one mma.sync m16n8k16 — the contraction is a
-// real (16 x d) x (d x keys) product, tiny next to the K/V stream it rides on.
-//   * one thread issues two TMA loads (K tile, V tile; 128-byte swizzle) into
-//     shared memory on two mbarriers; 64 KB per CTA at d = 128 lets three CTAs
-//     share an SM, so one CTA's loads overlap the others' arithmetic;
-//   * each of the 4 warps takes 32 keys: S = Q K^T (Q fragments from global,
-//     K fragments by ldmatrix), an exact softmax over its 32 keys (max, exp2 of
-//     the folded scale, sum via quad shuffles), P kept in registers as the A
-//     operand of O = P V (V fragments by ldmatrix.trans);
+// Work unit = (batch, KV head, run of cpc consecutive chunks of 128 keys). The
+// rows of a unit are all query rows that read this KV head: R = G * N_q <= 16
+// (G = H_q / H_kv, GQA), which is exactly the M = 16 of one mma.sync m16n8k16 —
+// the contraction is a real (16 x d) x (d x keys) product, tiny next to the K/V
+// stream it rides on.
+//   * one thread issues the TMA loads (K tile, V tile; 128-byte swizzle) into
+//     shared memory on two mbarriers, the next chunk's K as soon as every warp
+//     has used the current one (overlapping this chunk's PV), its V after PV;
+//     64 KB per CTA at d = 128 lets three CTAs share an SM;
+//   * each of the 4 warps takes 32 keys of every chunk: S = Q K^T (Q fragments
+//     from global, K fragments by ldmatrix), the online softmax over its keys
+//     across the unit's chunks (running max and sum, exact rescale of its
+//     accumulator in registers), P kept in registers as the A operand of
+//     O += P V (V fragments by ldmatrix.trans);
 //   * the 4 warps' (m, l, O) are merged in shared memory into one partial per
-//     (row, chunk); fa_decode_merge_kernel merges the chunks of each row.
+//     (row, unit); fa_decode_merge_kernel merges the units of each row.
 // The kernel is bound by HBM bandwidth: algorithmic bytes are K and V once per
 // KV head, Q read and O, LSE written once.
 #include "fa_internal.h"
@@ -91,10 +94,11 @@ __global__ void __launch_bounds__(kDecThreads)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int chunk = blockIdx.x % p.n_chunks;
-  const int bhk = blockIdx.x / p.n_chunks;
+  const int part = blockIdx.x % p.n_parts;
+  const int bhk = blockIdx.x / p.n_parts;
   const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
-  const int key0 = chunk * kDecKeys;
+  const int c_begin = part * p.cpc;
+  const int nc = min(p.n_chunks, c_begin + p.cpc) - c_begin;   // >= 1
 
   if (threadIdx.x == 0) {
     mbar_init(barK, 1);
@@ -102,15 +106,15 @@ __global__ void __launch_bounds__(kDecThreads)
     fence_mbar_init();
   }
   __syncthreads();
+  auto load = [&](uint32_t bar, uint32_t off, const CUtensorMap* tm, int chunk) {
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxes; ++bx)
+      tma_load_3d(sb + off + bx * C::kBoxBytes, tm, bar, bx * 64, chunk * kDecKeys, bhk);
+  };
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(barK, C::kTileBytes);
-#pragma unroll
-    for (int bx = 0; bx < C::kBoxes; ++bx)
-      tma_load_3d(sb + C::kOffK + bx * C::kBoxBytes, &tmK, barK, bx * 64, key0, bhk);
-    mbar_arrive_expect_tx(barV, C::kTileBytes);
-#pragma unroll
-    for (int bx = 0; bx < C::kBoxes; ++bx)
-      tma_load_3d(sb + C::kOffV + bx * C::kBoxBytes, &tmV, barV, bx * 64, key0, bhk);
+    load(barK, C::kOffK, &tmK, c_begin);
+    load(barV, C::kOffV, &tmV, c_begin);
   }
 
   // Q fragments (A operand, rows = the R query rows of this KV head, zero-padded to 16)
@@ -138,99 +142,129 @@ __global__ void __launch_bounds__(kDecThreads)
     }
   }
 
-  const int kw = warp * 32;  // this warp's 32 keys within the chunk
-  bool ok = mbar_wait(barK, 0, &abort_flag, p.status);
-  // ---- S = Q K^T for 32 keys: 4 n-tiles of 8 keys
-  float sacc[4][4];
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-  if (ok) {
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {   // pairs of n-tiles
-        const int i = lane >> 3, rr = lane & 7;
-        const int key = kw + 16 * np + 8 * (i >> 1) + rr;
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(sw128_addr(sb + C::kOffK, key, 2 * ks + (i & 1)), b00, b01, b10, b11);
-        mma16816(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-        mma16816(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
-      }
-    }
-  }
-  // ---- exact softmax over this warp's 32 keys, rows g and g + 8
+  const int kw = warp * 32;  // this warp's 32 keys within each chunk
   const float c = p.c;
-  float mrow[2], lrow[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int m = g + 8 * u;
-    const int i = (m < p.R) ? m % p.N_q : 0;
-    int lim = p.N_k - key0;                                  // keys of this chunk that exist
-    if (p.causal) lim = min(lim, i + p.kv_off + 1 - key0);   // ... and that row i may see
-    if (m >= p.R) lim = 0;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kw + 8 * nt + 2 * t + e;
-        float& sv = sacc[nt][2 * u + e];
-        if (key >= lim) sv = -INFINITY;
-        mx = fmaxf(mx, sv);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mb = (mx == -INFINITY) ? 0.f : mx * c;
-    float l = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float& sv = sacc[nt][2 * u + e];
-        sv = ex2_approx(fmaf(sv, c, -mb));
-        l += sv;
-      }
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    mrow[u] = (mx == -INFINITY) ? -INFINITY : mb;   // scaled log2 units
-    lrow[u] = l;
-  }
-  // P as the A operand of O = P V: k-step j covers keys kw + 16j .. kw + 16j + 15
-  uint32_t pa[2][4];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    pa[j][0] = pack_bf16x2(sacc[2 * j][0], sacc[2 * j][1]);
-    pa[j][1] = pack_bf16x2(sacc[2 * j][2], sacc[2 * j][3]);
-    pa[j][2] = pack_bf16x2(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
-    pa[j][3] = pack_bf16x2(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
-  }
-  // ---- O = P V: D/8 n-tiles of 8 columns
+  // running (m, l) of rows g and g + 8 over this warp's keys (m in scaled log2 units)
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   float oacc[D / 8][4];
 #pragma unroll
   for (int dn = 0; dn < D / 8; ++dn)
 #pragma unroll
     for (int e = 0; e < 4; ++e) oacc[dn][e] = 0.f;
-  if (ok) ok = mbar_wait(barV, 0, &abort_flag, p.status);
-  if (ok) {
+  int k_loads = 1, v_loads = 1;   // loads issued (thread 0), for the drain on failure
+  bool ok = true;
+  for (int ci = 0; ci < nc; ++ci) {
+    const int key0 = (c_begin + ci) * kDecKeys;
+    const uint32_t ph = (uint32_t)ci & 1u;
+    // ---- S = Q K^T for 32 keys: 4 n-tiles of 8 keys
+    const bool okK = mbar_wait(barK, ph, &abort_flag, p.status);
+    float sacc[4][4];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {   // pairs of d n-tiles
-        const int i = lane >> 3, rr = lane & 7;
-        const int key = kw + 16 * j + 8 * (i & 1) + rr;
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4_t(sw128_addr(sb + C::kOffV, key, 2 * dp + (i >> 1)), b00, b01, b10, b11);
-        mma16816(oacc[2 * dp], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b00, b01);
-        mma16816(oacc[2 * dp + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b10, b11);
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    if (okK) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {   // pairs of n-tiles
+          const int i = lane >> 3, rr = lane & 7;
+          const int key = kw + 16 * np + 8 * (i >> 1) + rr;
+          uint32_t b00, b01, b10, b11;
+          ldsm_x4(sw128_addr(sb + C::kOffK, key, 2 * ks + (i & 1)), b00, b01, b10, b11);
+          mma16816(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
+          mma16816(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+        }
       }
     }
-  } else {
-    // a load never arrived: wait (bounded) for any copy in flight before the CTA exits
+    // every warp is done with this K tile: the next chunk's may load (uniform ok)
+    ok = __syncthreads_and(okK) != 0;
+    if (!ok) break;
+    if (threadIdx.x == 0 && ci + 1 < nc) {
+      load(barK, C::kOffK, &tmK, c_begin + ci + 1);
+      ++k_loads;
+    }
+    // ---- online softmax over this warp's 32 keys, rows g and g + 8
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int m = g + 8 * u;
+      const int i = (m < p.R) ? m % p.N_q : 0;
+      int lim = p.N_k - key0;                                  // keys of this chunk that exist
+      if (p.causal) lim = min(lim, i + p.kv_off + 1 - key0);   // ... and that row i may see
+      if (m >= p.R) lim = 0;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = kw + 8 * nt + 2 * t + e;
+          float& sv = sacc[nt][2 * u + e];
+          if (key >= lim) sv = -INFINITY;
+          mx = fmaxf(mx, sv);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(mrow[u], mx == -INFINITY ? -INFINITY : mx * c);
+      // nothing seen yet: nothing to rescale; otherwise 2^(m_old - m_new) (0 from -inf)
+      const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(mrow[u] - m_new);
+      const float mb = (m_new == -INFINITY) ? 0.f : m_new;
+      float l = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float& sv = sacc[nt][2 * u + e];
+          sv = ex2_approx(fmaf(sv, c, -mb));
+          l += sv;
+        }
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      lrow[u] = lrow[u] * alpha + l;
+      mrow[u] = m_new;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        oacc[dn][2 * u] *= alpha;
+        oacc[dn][2 * u + 1] *= alpha;
+      }
+    }
+    // P as the A operand of O = P V: k-step j covers keys kw + 16j .. kw + 16j + 15
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      pa[j][0] = pack_bf16x2(sacc[2 * j][0], sacc[2 * j][1]);
+      pa[j][1] = pack_bf16x2(sacc[2 * j][2], sacc[2 * j][3]);
+      pa[j][2] = pack_bf16x2(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
+      pa[j][3] = pack_bf16x2(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+    }
+    // ---- O += P V: D/8 n-tiles of 8 columns
+    const bool okV = mbar_wait(barV, ph, &abort_flag, p.status);
+    if (okV) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {   // pairs of d n-tiles
+          const int i = lane >> 3, rr = lane & 7;
+          const int key = kw + 16 * j + 8 * (i & 1) + rr;
+          uint32_t b00, b01, b10, b11;
+          ldsm_x4_t(sw128_addr(sb + C::kOffV, key, 2 * dp + (i >> 1)), b00, b01, b10, b11);
+          mma16816(oacc[2 * dp], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b00, b01);
+          mma16816(oacc[2 * dp + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b10, b11);
+        }
+      }
+    }
+    // every warp is done with this V tile: the next chunk's may load
+    ok = __syncthreads_and(okV) != 0;
+    if (!ok) break;
+    if (threadIdx.x == 0 && ci + 1 < nc) {
+      load(barV, C::kOffV, &tmV, c_begin + ci + 1);
+      ++v_loads;
+    }
+  }
+  if (!ok && threadIdx.x == 0) {
+    // a wait gave up: let every load issued land (bounded) before the CTA exits
     volatile int never = 0;
-    mbar_wait(barK, 0, &never, p.status);
-    mbar_wait(barV, 0, &never, p.status);
+    mbar_wait(barK, (uint32_t)(k_loads - 1) & 1u, &never, p.status);
+    mbar_wait(barV, (uint32_t)(v_loads - 1) & 1u, &never, p.status);
   }
 
   // ---- merge the 4 warps' partials in shared memory (the K tile is dead now)
@@ -251,7 +285,7 @@ __global__ void __launch_bounds__(kDecThreads)
   }
   __syncthreads();
   // each partial row: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w 2^(m_w - M) O_w
-  const size_t pbase = ((size_t)bhk * p.n_chunks + chunk) * p.R;
+  const size_t pbase = ((size_t)bhk * p.n_parts + part) * p.R;
   for (int idx = threadIdx.x; idx < p.R * D; idx += kDecThreads) {
     const int m = idx / D, dcol = idx - m * D;
     float M = -INFINITY;
@@ -292,11 +326,11 @@ __global__ void __launch_bounds__(D) fa_decode_merge_kernel(const DecParams p) {
   const int hl = m / p.N_q, i = m - hl * p.N_q;
   const int hq = hk * p.G + hl;
   const size_t stride = (size_t)p.R;                     // between chunks of one row
-  const size_t base = (size_t)bhk * p.n_chunks * p.R + m;
+  const size_t base = (size_t)bhk * p.n_parts * p.R + m;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   // pass 1: M = max over chunks with l > 0
   float M = -INFINITY;
-  for (int ch = tid; ch < p.n_chunks; ch += D) {
+  for (int ch = tid; ch < p.n_parts; ch += D) {
     const float2 v = __ldcg(ml + base + ch * stride);
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
@@ -313,8 +347,8 @@ __global__ void __launch_bounds__(D) fa_decode_merge_kernel(const DecParams p) {
   M = s_ML[0];
   float acc = 0.f, Lpart = 0.f;
   const float* src = p.part_o + base * D + tid;
-  for (int c0 = 0; c0 < p.n_chunks; c0 += kMergeMaxChunks) {
-    const int nc = min(kMergeMaxChunks, p.n_chunks - c0);
+  for (int c0 = 0; c0 < p.n_parts; c0 += kMergeMaxChunks) {
+    const int nc = min(kMergeMaxChunks, p.n_parts - c0);
     // pass 2: unnormalised weights of this group of chunks
     for (int ch = tid; ch < nc; ch += D) {
       const float2 v = __ldcg(ml + base + (size_t)(c0 + ch) * stride);
@@ -365,7 +399,7 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const long long ctas = (long long)p.B * p.H_kv * p.n_chunks;
+  const long long ctas = (long long)p.B * p.H_kv * p.n_parts;
   fa_decode_kernel<D><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -384,13 +418,23 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
 
 }  // namespace
 
-size_t decode_part_bytes(int B, int H_kv, int R, int n_chunks, int d) {
-  return (size_t)B * H_kv * n_chunks * R * ((size_t)d * 4 + 8);
+size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d) {
+  return (size_t)B * H_kv * n_parts * R * ((size_t)d * 4 + 8);
+}
+
+int decode_chunks_per_cta(long long heads, int n_chunks, int sms) {
+  // the largest run (power of two, at most 16 chunks) that still leaves four
+  // waves of CTAs (three per SM) to keep HBM busy to the end
+  int cpc = 1;
+  while (cpc < 16 && cpc * 2 <= n_chunks &&
+         heads * ((n_chunks + 2 * cpc - 1) / (2 * cpc)) >= 4ll * 3 * sms)
+    cpc *= 2;
+  return cpc;
 }
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
                           cudaStream_t stream) {
-  if ((long long)p.B * p.H_kv * p.n_chunks <= 0) return cudaSuccess;
+  if ((long long)p.B * p.H_kv * p.n_parts <= 0) return cudaSuccess;
   return d == 128 ? launch_decode_t<128>(tk, tv, p, stream) : launch_decode_t<64>(tk, tv, p, stream);
 }
 

@@ -69,15 +69,19 @@ struct DecParams {
   int G, R;          // G = H_q / H_kv; R = G * N_q query rows per (batch, KV head)
   int causal, kv_off;
   int n_chunks;      // ceil(N_k / 128)
+  int cpc;           // chunks per CTA (a run of consecutive chunks)
+  int n_parts;       // ceil(n_chunks / cpc): CTAs, and partials, per (batch, KV head)
   float c;           // scale * log2(e)
   const __nv_bfloat16* q;  // [B][H_q][N_q][d]
   void* o;
   float* lse;
-  float* part_o;     // fp32 [B*H_kv][n_chunks][R][d]
-  float* part_ml;    // fp32 [B*H_kv][n_chunks][R][2]
+  float* part_o;     // fp32 [B*H_kv][n_parts][R][d]
+  float* part_ml;    // fp32 [B*H_kv][n_parts][R][2]
   int* status;
 };
-size_t decode_part_bytes(int B, int H_kv, int R, int n_chunks, int d);
+size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d);
+// Chunks per decode CTA for `heads` = B * H_kv KV heads of n_chunks chunks each.
+int decode_chunks_per_cta(long long heads, int n_chunks, int sms);
 // Launch the decode kernel, then the chunk merge as its programmatic dependent.
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
                           cudaStream_t stream);

@@ -60,6 +60,9 @@ SMALL = [
     (1, 2, 2, 16, 16, 64, True),        # square causal inside one chunk
     (1, 2, 1, 8, 5, 128, True),         # N_q > N_k: leading rows see no key
     (3, 8, 8, 1, 128, 128, False),      # exactly one chunk
+    # decode CTAs that walk runs of chunks (128 KV heads: runs of 2 chunks, ragged last run)
+    (8, 32, 16, 4, 4100, 128, True),    # GQA 2 x 4 queries, causal
+    (16, 8, 8, 1, 4200, 64, False),     # MQA-free, d = 64
 ]
 
 
