@@ -326,23 +326,28 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     p.causal = causal ? 1 : 0;
     p.kv_off = N_k - N_q;
     p.n_chunks = (N_k + 127) / 128;
-    p.cpc = decode_chunks_per_cta((long long)B * H_kv, p.n_chunks, num_sms());
-    p.n_parts = (p.n_chunks + p.cpc - 1) / p.cpc;
+    const DecPlan dp = decode_plan((long long)B * H_kv, p.n_chunks, d, num_sms(), cluster_merge_enabled());
+    p.cpc = dp.cpc;
+    p.n_parts = dp.n_parts;
+    p.cm = dp.cm;
     p.c = scale * 1.4426950408889634f;
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.o = o;
     p.lse = lse;
     p.status = status;
     if ((long long)B * H_kv * p.n_parts >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-    const size_t bytes = decode_part_bytes(B, H_kv, p.R, p.n_parts, d);
+    const size_t bytes = p.cm ? 0 : decode_part_bytes(B, H_kv, p.R, p.n_parts, d);
     void* ws = nullptr;
-    st = wsrc.acquire(bytes, strm, &ws);
-    if (st != FA_OK) return st;
+    if (bytes > 0) {
+      st = wsrc.acquire(bytes, strm, &ws);
+      if (st != FA_OK) return st;
+    }
     p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                         (size_t)B * H_kv * p.n_parts * p.R * d * 4);
+    p.part_ml = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                              (size_t)B * H_kv * p.n_parts * p.R * d * 4)
+                   : nullptr;
     cudaError_t e = launch_decode(d, tk, tv, p, strm);
-    if (wsrc.release) wsrc.release(ws, strm);
+    if (ws && wsrc.release) wsrc.release(ws, strm);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
   }
 
@@ -450,11 +455,11 @@ int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causa
     n = 1;
   } else if ((long long)(H_q / H_kv) * N_q <= fa::kDecodeMaxRows) {
     const int chunks = (N_k + 127) / 128;
-    const int cpc = fa::decode_chunks_per_cta((long long)B * H_kv, chunks, fa::num_sms());
-    const int parts = (chunks + cpc - 1) / cpc;
-    c = (long long)B * H_kv * parts;
-    n = 2;
-    ws = fa::decode_part_bytes(B, H_kv, (H_q / H_kv) * N_q, parts, d);
+    const fa::DecPlan dp = fa::decode_plan((long long)B * H_kv, chunks, d, fa::num_sms(),
+                                           fa::cluster_merge_enabled());
+    c = (long long)B * H_kv * dp.n_parts;
+    n = dp.cm ? 1 : 2;
+    ws = dp.cm ? 0 : fa::decode_part_bytes(B, H_kv, (H_q / H_kv) * N_q, dp.n_parts, d);
   } else {
     const fa::FwdPlan pl = fa::prefill_plan(B, H_q, N_q, N_k, d, causal);
     c = pl.units;

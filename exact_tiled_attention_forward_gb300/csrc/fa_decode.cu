@@ -43,8 +43,12 @@ struct DecCfg {
   static constexpr int kTileBytes = kDecKeys * D * 2;       // K or V chunk
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
-  static constexpr int kOffMl = 2 * kTileBytes;             // [4 warps][16 rows][2] f32
-  static constexpr int kOffBar = kOffMl + 4 * 16 * 2 * 4;
+  // [4 warps][16 rows][2] f32 (m, l); later [16][8] merge weights + [16][2] (M, L)
+  static constexpr int kMlFloats = 16 * 8 + 16 * 2;
+  static constexpr int kOffMl = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffMl + kMlFloats * 4;
+  static_assert(4 * 16 * 2 <= kMlFloats, "the warps' (m, l) must fit");
+  static_assert(16 * D * 4 + 16 * 2 * 4 <= kTileBytes, "a CTA's partial must fit in the V tile");
   static constexpr int kSmemBytes = kOffBar + 16 + 1024;
   // merge buffer [4 warps][16 rows][D] f32 reuses the K tile (dead after S = Q K^T)
   static_assert(4 * 16 * D * 4 <= kTileBytes, "merge buffer must fit in the K tile");
@@ -286,6 +290,10 @@ __global__ void __launch_bounds__(kDecThreads)
   __syncthreads();
   // each partial row: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w 2^(m_w - M) O_w
   const size_t pbase = ((size_t)bhk * p.n_parts + part) * p.R;
+  // this CTA's combined partial, kept in shared memory for the in-cluster merge
+  // (the V tile is dead after the last PV): [16][D] O, then [16][2] (m, l)
+  float* cpo = reinterpret_cast<float*>(smem + C::kOffV);
+  float* cml = cpo + 16 * D;
   for (int idx = threadIdx.x; idx < p.R * D; idx += kDecThreads) {
     const int m = idx / D, dcol = idx - m * D;
     float M = -INFINITY;
@@ -302,9 +310,86 @@ __global__ void __launch_bounds__(kDecThreads)
         acc += wt * mo[((size_t)w * 16 + m) * D + dcol];
       }
     }
-    __stcg(p.part_o + (pbase + m) * D + dcol, acc);
-    if (dcol == 0) __stcg(reinterpret_cast<float2*>(p.part_ml) + pbase + m, make_float2(L > 0.f ? M : -INFINITY, L));
+    if (p.cm) {
+      cpo[m * D + dcol] = acc;
+      if (dcol == 0) {
+        cml[2 * m] = L > 0.f ? M : -INFINITY;
+        cml[2 * m + 1] = L;
+      }
+    } else {
+      __stcg(p.part_o + (pbase + m) * D + dcol, acc);
+      if (dcol == 0)
+        __stcg(reinterpret_cast<float2*>(p.part_ml) + pbase + m, make_float2(L > 0.f ? M : -INFINITY, L));
+    }
   }
+  if (!p.cm) return;
+
+  // ---- in-cluster merge: the n_parts CTAs of this KV head form one cluster
+  // (rank = part); rank 0 combines the parts' partials from their shared memory
+  // and writes O and LSE (page 2, "The Tiling Algorithm", applied to whole runs)
+  cluster_sync();   // every part's partial is in its shared memory
+  if (part == 0) {
+    float* sw = mml;   // [16 rows][8 parts] weights 2^(m_p - M) / L (the warps' (m, l) are dead)
+    float* sML = mml + 16 * 8;   // [16][2] (M, L) per row
+    if (threadIdx.x < p.R) {
+      const int m = threadIdx.x;
+      float mp[8], lp[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {   // all remote loads in flight at once
+        mp[q] = -INFINITY;
+        lp[q] = 0.f;
+        if (q < p.n_parts) {
+          const float2 v = ld_cluster_v2f(mapa_shared(smem_u32(cml + 2 * m), (uint32_t)q));
+          mp[q] = v.x;
+          lp[q] = v.y;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (lp[q] > 0.f) M = fmaxf(M, mp[q]);
+      float L = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float w = lp[q] > 0.f ? ex2_approx(mp[q] - M) : 0.f;
+        mp[q] = w;
+        L += w * lp[q];
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sw[m * 8 + q] = mp[q] * inv;
+      sML[2 * m] = M;
+      sML[2 * m + 1] = L;
+    }
+    __syncthreads();
+    // four consecutive columns per thread, one float4 from every part in flight at once
+    for (int idx = threadIdx.x * 4; idx < p.R * D; idx += kDecThreads * 4) {
+      const int m = idx / D, dcol = idx - m * D;
+      float4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = q < p.n_parts ? ld_cluster_v4f(mapa_shared(smem_u32(cpo + m * D + dcol), (uint32_t)q))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float w = sw[m * 8 + q];   // 0 for q >= n_parts
+        acc.x += w * v[q].x; acc.y += w * v[q].y; acc.z += w * v[q].z; acc.w += w * v[q].w;
+      }
+      const int hl = m / p.N_q, i = m - hl * p.N_q;
+      const int hq = hk * p.G + hl;
+      const size_t orow = ((size_t)b * p.H_q + hq) * p.N_q + i;
+      uint2 o2;
+      o2.x = pack_bf16x2(acc.x, acc.y);
+      o2.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow * D + dcol) = o2;
+      if (dcol == 0 && p.lse) {
+        const float L = sML[2 * m + 1];
+        p.lse[orow] = L > 0.f ? (sML[2 * m] + __log2f(L)) * kLn2d : -INFINITY;
+      }
+    }
+  }
+  cluster_sync();   // rank 0 has read every part's shared memory
 }
 
 // Merge of the chunk partials of each query row (same algebra as the prefill
@@ -400,9 +485,27 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
     attr = true;
   }
   const long long ctas = (long long)p.B * p.H_kv * p.n_parts;
-  fa_decode_kernel<D><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (p.cm && p.n_parts > 1) {
+    // the parts of one KV head run as one cluster and merge in the kernel
+    cudaLaunchConfig_t kc{};
+    kc.gridDim = dim3((unsigned)ctas);
+    kc.blockDim = dim3(kDecThreads);
+    kc.dynamicSmemBytes = C::kSmemBytes;
+    kc.stream = stream;
+    cudaLaunchAttribute ka[1];
+    ka[0].id = cudaLaunchAttributeClusterDimension;
+    ka[0].val.clusterDim.x = (unsigned)p.n_parts;
+    ka[0].val.clusterDim.y = 1;
+    ka[0].val.clusterDim.z = 1;
+    kc.attrs = ka;
+    kc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&kc, fa_decode_kernel<D>, tk, tv, p);
+  } else {
+    fa_decode_kernel<D><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess || p.cm) return e;
   const long long rows = (long long)p.B * p.H_kv * p.R;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)rows);
@@ -422,14 +525,67 @@ size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d) {
   return (size_t)B * H_kv * n_parts * R * ((size_t)d * 4 + 8);
 }
 
-int decode_chunks_per_cta(long long heads, int n_chunks, int sms) {
-  // the largest run (power of two, at most 16 chunks) that still leaves four
-  // waves of CTAs (three per SM) to keep HBM busy to the end
+template <int D>
+int decode_cluster_capacity_t(int parts) {
+  using C = DecCfg<D>;
+  if (cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)parts);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)parts;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fa_decode_kernel<D>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+DecPlan decode_plan(long long heads, int n_chunks, int d, int sms, bool cluster_merge) {
+  DecPlan pl{};
+  // in-cluster merge: the fewest parts (at most 8, a portable cluster) that keep
+  // two waves of CTAs (three per SM); when no such count exists but a KV head has
+  // at most 8 chunks, one part per chunk (the GPU cannot be filled anyway). One
+  // part needs no merge at all.
+  if (cluster_merge) {
+    int parts = 0;
+    const int qmax = n_chunks < 8 ? n_chunks : 8;
+    for (int q = 1; q <= qmax && parts == 0; ++q)
+      if (heads * q >= 2ll * 3 * sms) parts = q;
+    if (parts == 0 && n_chunks <= 8) parts = n_chunks;
+    if (parts > 0) {
+      const int cpc = (n_chunks + parts - 1) / parts;
+      const int np = (n_chunks + cpc - 1) / cpc;
+      if (np == 1 ||
+          (d == 128 ? decode_cluster_capacity_t<128>(np) : decode_cluster_capacity_t<64>(np)) > 0) {
+        pl.cpc = cpc;
+        pl.n_parts = np;
+        pl.cm = 1;
+        return pl;
+      }
+    }
+  }
+  // otherwise: the largest run (power of two, at most 16 chunks) that still leaves
+  // four waves of CTAs to keep HBM busy to the end; a merge kernel combines the runs
   int cpc = 1;
   while (cpc < 16 && cpc * 2 <= n_chunks &&
          heads * ((n_chunks + 2 * cpc - 1) / (2 * cpc)) >= 4ll * 3 * sms)
     cpc *= 2;
-  return cpc;
+  pl.cpc = cpc;
+  pl.n_parts = (n_chunks + cpc - 1) / cpc;
+  pl.cm = pl.n_parts == 1 ? 1 : 0;
+  return pl;
 }
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,

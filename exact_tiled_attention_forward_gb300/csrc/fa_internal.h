@@ -71,6 +71,7 @@ struct DecParams {
   int n_chunks;      // ceil(N_k / 128)
   int cpc;           // chunks per CTA (a run of consecutive chunks)
   int n_parts;       // ceil(n_chunks / cpc): CTAs, and partials, per (batch, KV head)
+  int cm;            // 1: the n_parts CTAs of a KV head form a cluster and merge in-kernel
   float c;           // scale * log2(e)
   const __nv_bfloat16* q;  // [B][H_q][N_q][d]
   void* o;
@@ -80,8 +81,11 @@ struct DecParams {
   int* status;
 };
 size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d);
-// Chunks per decode CTA for `heads` = B * H_kv KV heads of n_chunks chunks each.
-int decode_chunks_per_cta(long long heads, int n_chunks, int sms);
+// How the decode kernel cuts `heads` = B * H_kv KV heads of n_chunks chunks each.
+struct DecPlan {
+  int cpc, n_parts, cm;   // chunks per CTA, CTAs per KV head, in-cluster merge
+};
+DecPlan decode_plan(long long heads, int n_chunks, int d, int sms, bool cluster_merge);
 // Launch the decode kernel, then the chunk merge as its programmatic dependent.
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
                           cudaStream_t stream);

@@ -82,6 +82,7 @@ SPLIT = [
     (1, 1, 1, 2000, 3000, 64, False),    # ragged, d = 64, eight key ranges
     (2, 3, 1, 700, 1500, 128, True),     # causal, GQA, unequal ranges inside a cluster
     (1, 1, 1, 256, 2048, 128, False),    # a single block
+    (16, 32, 8, 1, 8192, 128, False),    # decode: runs of chunks per KV head, merged either way
 ]
 
 
