@@ -267,7 +267,8 @@ def time_decode(fa, torch, dev, flush, stream, steps, warmup, world):
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    return {"ms": ms, "gbs": world * a_bytes / 1e9 / (ms * 1e-3), "bytes": a_bytes}
+    return {"ms": ms, "gbs": world * a_bytes / 1e9 / (ms * 1e-3), "bytes": a_bytes,
+            "launches": fused_launches_per_step(fa, cfg)}
 
 
 def main():
@@ -488,8 +489,9 @@ def main():
                          "frac": decode["gbs"] / float(peaks["hbm_gbs"]),
                          "traffic": profiled_traffic(DECODE_WORKLOAD, "fa_decode_kernel"),
                          "algorithmic_per_launch": decode["bytes"],
-                         "kernel": "fa_decode_kernel + fa_decode_merge_kernel"},
-            "gpu_launches": 2 * args.decode_steps},
+                         "kernel": ("fa_decode_kernel (in-cluster merge)" if decode["launches"] == 1
+                                    else "fa_decode_kernel + fa_decode_merge_kernel")},
+            "gpu_launches": decode["launches"] * args.decode_steps},
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
