@@ -34,6 +34,7 @@ os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 import numpy as np  # noqa: E402
 
 from exact_tiled_attention_forward_gb300 import inputs as I  # noqa: E402
+from exact_tiled_attention_forward_gb300 import replicas as R  # noqa: E402
 from exact_tiled_attention_forward_gb300 import work as W  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofline"
@@ -262,12 +263,8 @@ def time_decode(fa, torch, dev, flush, stream, steps, warmup, world):
         fa.fa_forward(q, k, v, causal=False, scale=a.scale, out=o, lse=lse)
         e1.record(stream)
     torch.cuda.synchronize()
-    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"ms": ms, "gbs": world * a_bytes / 1e9 / (ms * 1e-3), "bytes": a_bytes,
+    ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps, world, dev)
+    return {"ms": ms, "gbs": R.whole_job_rate(a_bytes / 1e9, 1, ms, world), "bytes": a_bytes,
             "launches": fused_launches_per_step(fa, cfg)}
 
 
@@ -285,8 +282,7 @@ def main():
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank, world, local = R.replica_env()
     cfg, a_flops, a_bytes, decode_cfg = workload_config(args.workload)
     unit = "GB/s" if decode_cfg else "TFLOP/s"
     work_per_step = (a_bytes / 1e9) if decode_cfg else (a_flops / 1e12)
@@ -326,7 +322,6 @@ def main():
 
     if world > 1:
         import torch.distributed as dist
-        local = int(os.environ.get("LOCAL_RANK", "0"))
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -390,13 +385,9 @@ def main():
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = R.slowest_rank_ms(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * work_per_step * args.steps / (total_ms * 1e-3)
+    value = R.whole_job_rate(work_per_step, args.steps, total_ms, world)
     if fa.fa_device_status() != fa.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait during the benchmark")
 
@@ -426,12 +417,8 @@ def main():
         e2e_step()
         e1.record(stream)
     barrier()
-    e2e_ms = sum(e0.elapsed_time(e1) for e0, e1 in eev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * work_per_step * args.steps / (e2e_ms * 1e-3)
+    e2e_ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in eev), world, dev)
+    e2e_value = R.whole_job_rate(work_per_step, args.steps, e2e_ms, world)
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
 
