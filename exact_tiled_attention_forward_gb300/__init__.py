@@ -53,6 +53,7 @@ _SIGNATURES = {
     "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
     "fa_forward_plan": (_c_int, [_c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong),
                                                 ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
+    "fa_selftest_wait_timeout": (_c_int, [ctypes.c_ulonglong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_get_last_cuda_error": (_c_int, []),
     "fa_device_status": (_c_int, [_c_int]),

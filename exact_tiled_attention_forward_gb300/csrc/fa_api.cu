@@ -267,6 +267,9 @@ int* device_status_ptr() {
 namespace {
 
 int pool_acquire(size_t bytes, cudaStream_t stream, void** ptr) {
+  // test hook: FA_TEST_WORKSPACE_FAIL=1 makes every workspace allocation fail
+  const char* fail = getenv("FA_TEST_WORKSPACE_FAIL");
+  if (fail && fail[0] == '1') return FA_ERR_NO_MEMORY;
   cudaMemPool_t pool = workspace_pool();
   if (!pool) return cuda_fail(cudaGetLastError());
   cudaError_t e = cudaMallocFromPoolAsync(ptr, bytes, pool, stream);

@@ -62,16 +62,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete. Returns false (and
 // raises *abort, records FA_DEV_TIMEOUT in *status) if it does not complete
-// within FA_WAIT_TIMEOUT_NS, or if another thread of the CTA raised *abort.
+// within timeout_ns (FA_WAIT_TIMEOUT_NS in the kernels), or if another thread
+// of the CTA raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, uint64_t timeout_ns = FA_WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         *abort = 1;
         if (status) atomicCAS(status, FA_DEV_OK, FA_DEV_TIMEOUT);
         return false;

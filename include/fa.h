@@ -73,7 +73,9 @@ typedef enum {
  * Split and decode partials live in a stream-ordered workspace taken from a
  * library-owned memory pool on the current device (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`); the pool keeps freed memory reserved for later
- * calls until the process exits. No pointer outlives the call.
+ * calls until the process exits. No pointer outlives the call. With
+ * FA_TEST_WORKSPACE_FAIL=1 in the environment every workspace allocation fails
+ * (FA_ERR_NO_MEMORY, nothing enqueued): a hook to test that error path.
  * Returns FA_OK or an fa_status code. */
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream);
@@ -131,6 +133,16 @@ size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k);
  * FA_ERR_UNSUPPORTED. */
 int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal, long long* ctas,
                     int* launches, size_t* workspace_bytes);
+
+/* Failure-detection self-test (no counterpart on the pages; the kernels'
+ * bounded waits are what it exercises). Enqueues on `stream` one CTA that runs
+ * the same bounded mbarrier wait the kernels use, on a barrier nothing ever
+ * arrives at, with a limit of timeout_ns (1 ns .. 10 s) instead of the kernels'
+ * 2 s: the wait gives up, records FA_ERR_TIMEOUT in the device status word and
+ * the kernel returns, leaving the context usable. Read the result with
+ * fa_device_status. Returns FA_OK once enqueued, FA_ERR_INVALID_ARG for a limit
+ * out of range, FA_ERR_CUDA on a launch failure. */
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 
 /* Static description of an fa_status code. Never NULL. */
 const char* fa_status_string(int status);

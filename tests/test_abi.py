@@ -26,7 +26,7 @@ def lib():
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
     assert set(names) == {"fa_forward", "fa_forward_noalloc", "fa_naive_forward",
-                          "fa_naive_workspace_bytes", "fa_forward_plan",
+                          "fa_naive_workspace_bytes", "fa_forward_plan", "fa_selftest_wait_timeout",
                           "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
                           "fa_version"}
     for n in names:
@@ -114,3 +114,9 @@ def test_no_gpu_fails_loudly(lib):
         pytest.skip("GPU present")
     # a valid request on a machine without a GPU is a CUDA error, never a silent success
     assert _fwd(lib) == fa.FA_ERR_CUDA
+
+
+def test_selftest_rejects_limits_out_of_range(lib):
+    # argument checks come before any CUDA call
+    assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_wait_timeout(20_000_000_000, None) == fa.FA_ERR_INVALID_ARG

@@ -25,13 +25,37 @@ def fa():
     return fa
 
 
-def _run(fa, a, naive=False):
-    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
-    fn = fa.fa_naive_forward if naive else fa.fa_forward
-    o, lse = fn(q, k, v, causal=a.causal, scale=a.scale)
+GUARD = 4096   # elements of canary before and after O and LSE (16-byte multiples)
+
+
+def _guarded(torch, shape, dtype, fill):
+    """A tensor of `shape` inside a larger buffer whose margins hold `fill`."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def _margins_intact(buf, fill):
     import torch
+    n = buf.numel() - 2 * GUARD
+    ref = torch.full((GUARD,), fill, dtype=buf.dtype, device=buf.device)
+    return bool(torch.equal(buf[:GUARD], ref)) and bool(torch.equal(buf[GUARD + n:], ref))
+
+
+def _run(fa, a, naive=False):
+    """Run through the binding with O and LSE inside canary margins; the margins
+    must be untouched afterwards (no write outside the outputs)."""
+    import torch
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    B, H_q, H_kv, N_q, N_k, d = a.shape_args
+    ob, o = _guarded(torch, (B, H_q, N_q, d), torch.bfloat16, -12345.0)
+    lb, lse = _guarded(torch, (B, H_q, N_q), torch.float32, -12345.0)
+    fn = fa.fa_naive_forward if naive else fa.fa_forward
+    o2, lse2 = fn(q, k, v, causal=a.causal, scale=a.scale, out=o, lse=lse)
     torch.cuda.synchronize()
     assert fa.fa_device_status() == fa.FA_OK
+    assert o2.data_ptr() == o.data_ptr() and lse2.data_ptr() == lse.data_ptr()
+    assert _margins_intact(ob, -12345.0) and _margins_intact(lb, -12345.0)
     return bf16_dev_to_f64(o), lse.cpu().numpy().astype(np.float64)
 
 
