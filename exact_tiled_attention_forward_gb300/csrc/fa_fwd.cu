@@ -329,8 +329,9 @@ __device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int u) {
     }
   }
   const int n_all = max_i(kvh[0], kvh[1]);
-  ui.lo = (int)(((long long)ui.split * n_all) / ui.S);
-  const int hi = (int)(((long long)(ui.split + 1) * n_all) / ui.S);
+  // split * n_all < 2^29 (at most 16 splits of at most 2^24 key tiles): 32-bit division
+  ui.lo = (int)(((unsigned)ui.split * (unsigned)n_all) / (unsigned)ui.S);
+  const int hi = (int)(((unsigned)(ui.split + 1) * (unsigned)n_all) / (unsigned)ui.S);
   ui.n0 = max_i(0, min_i(hi, kvh[0]) - ui.lo);
   ui.n1 = max_i(0, min_i(hi, kvh[1]) - ui.lo);
   ui.nmax = max_i(ui.n0, ui.n1);
