@@ -363,6 +363,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // barriers first (the plain kernel's counts do not depend on the unit), so
+  // their set-up overlaps the parameter loads of the unit decode below
+  if (!MC && warp == kWarpProducer && lane == 0) {
+    mbar_init(bar(C::kBarQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarS + 0), 1);
+    mbar_init(bar(C::kBarS + 1), 1);
+    for (int X = 0; X < 2; ++X) {
+      mbar_init(bar(C::kBarP1 + X), 128);
+      mbar_init(bar(C::kBarP2 + X), 128);
+    }
+    mbar_init(bar(C::kBarO), 1);
+    mbar_init(bar(C::kBarDrain), 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+
   // ---- work unit. Units [0, u_full) are whole query blocks written directly;
   // the rest split the last query blocks' key ranges into s_tail parts whose
   // partial (m, l, O) go to the workspace (merged by fa_merge_kernel). Query
@@ -396,22 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up. The producer lane initialises the barriers and starts the Q
   // loads at once, so they overlap the rest of the set-up.
   if (warp == kWarpProducer && lane == 0) {
-    mbar_init(bar(C::kBarQ), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarFull + s), 1);
-      mbar_init(bar(C::kBarEmpty + s), share ? 2 : 1);   // both CTAs release a shared stage
+    if (MC) {
+      mbar_init(bar(C::kBarQ), 1);
+      for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(bar(C::kBarFull + s), 1);
+        mbar_init(bar(C::kBarEmpty + s), share ? 2 : 1);   // both CTAs release a shared stage
+      }
+      mbar_init(bar(C::kBarS + 0), 1);
+      mbar_init(bar(C::kBarS + 1), 1);
+      for (int X = 0; X < 2; ++X) {
+        mbar_init(bar(C::kBarP1 + X), 128);   // all 128 rows of the tile
+        mbar_init(bar(C::kBarP2 + X), 128);
+      }
+      mbar_init(bar(C::kBarO), 1);
+      mbar_init(bar(C::kBarDrain), 1);
+      *s_abort = 0;
+      fence_mbar_init();
+      fence_proxy_async_smem();
     }
-    mbar_init(bar(C::kBarS + 0), 1);
-    mbar_init(bar(C::kBarS + 1), 1);
-    for (int X = 0; X < 2; ++X) {
-      mbar_init(bar(C::kBarP1 + X), 128);   // all 128 rows of the tile
-      mbar_init(bar(C::kBarP2 + X), 128);
-    }
-    mbar_init(bar(C::kBarO), 1);
-    mbar_init(bar(C::kBarDrain), 1);
-    *s_abort = 0;
-    fence_mbar_init();
-    fence_proxy_async_smem();
     // the merge kernel (launched as a programmatic dependent) may be scheduled
     // once every CTA of this grid has started; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
