@@ -403,20 +403,28 @@ def main():
     warm_ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in wev), world, dev)
     warm_value = R.whole_job_rate(work_per_step, args.steps, warm_ms, world)
 
-    # ---- end to end through the public API with host buffers
-    pin = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hq, hk, hv = pin(a.q), pin(a.k), pin(a.v)
-    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # ---- end to end through the public API with host buffers: the step's inputs
+    # are staged in one pinned host buffer (Q | K | V) and its results read back
+    # from one device buffer (O | LSE), so each direction is a single copy over
+    # the host link (which tops out near 210 GB/s for pinned copies on this machine)
+    nq, nk = a.q.size, a.k.size
+    hin = torch.from_numpy(np.concatenate([a.q.reshape(-1), a.k.reshape(-1), a.v.reshape(-1)])
+                           .view(np.int16)).view(torch.bfloat16).pin_memory()
+    din = torch.empty_like(hin, device=dev)
+    dq, dk, dv = din[:nq].view(q.shape), din[nq:nq + nk].view(k.shape), din[nq + nk:].view(v.shape)
+    o_bytes, l_bytes = o.numel() * 2, lse.numel() * 4
+    dout = torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev)
+    hout = torch.empty(o_bytes + l_bytes, dtype=torch.uint8).pin_memory()
+    eo = dout[:o_bytes].view(torch.bfloat16).view(o.shape)
+    el = dout[o_bytes:].view(torch.float32).view(lse.shape)
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        step(dq, dk, dv)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        din.copy_(hin, non_blocking=True)
+        if ws is None:
+            fn(dq, dk, dv, causal=a.causal, scale=a.scale, out=eo, lse=el)
+        else:
+            fn(dq, dk, dv, causal=a.causal, scale=a.scale, out=eo, lse=el, workspace=ws)
+        hout.copy_(dout, non_blocking=True)
 
     for _ in range(warmup):
         e2e_step()
@@ -431,8 +439,8 @@ def main():
     barrier()
     e2e_ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in eev), world, dev)
     e2e_value = R.whole_job_rate(work_per_step, args.steps, e2e_ms, world)
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
-    d2h = ho.numel() * 2 + hl.numel() * 4
+    h2d = hin.numel() * 2
+    d2h = hout.numel()
 
     # ---- secondary half of the metric: decode HBM GB/s (batch 16, 32/8 heads, 8192 keys)
     decode = None
