@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -146,6 +147,24 @@ bool multicast_enabled() {
 bool cluster_merge_enabled() {
   const char* e = getenv("FA_CLUSTER_MERGE");
   return !(e && e[0] == '0');
+}
+
+// Causal block order (block_of in fa_fwd.cu): how many query heads run
+// interleaved, longest blocks first. As many as keep their K and V within half
+// of the L2 cache (64 MiB), counted in whole KV heads (the query heads that
+// share a KV head stay together). FA_CAUSAL_HEAD_GROUP=n (n >= 1) sets it
+// instead: a hook for tests of groups that do not divide the head count.
+int causal_head_group(int H_q, int H_kv, int N_k, int d, int n_bh) {
+  long long g = 0;
+  const char* e = getenv("FA_CAUSAL_HEAD_GROUP");
+  if (e && atoi(e) >= 1) {
+    g = atoi(e);
+  } else {
+    const long long kv_bytes = 4ll * N_k * d;   // K and V of one KV head, BF16
+    const long long kv_heads = std::max(1ll, (64ll << 20) / std::max(1ll, kv_bytes));
+    g = kv_heads * (H_q / H_kv);
+  }
+  return (int)std::min<long long>(std::max(1ll, g), (long long)n_bh);
 }
 
 int num_sms() {
@@ -372,6 +391,9 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.n_units = (int)pl.units;
   p.cm = pl.cluster_merge;
   const bool multicast = pl.n_tail == 0 && pl.units >= 2 && multicast_enabled();
+  p.n_bh = B * H_q;
+  // the multicast variant pairs adjacent blocks of one head: head-major there
+  p.hgroup = (causal && !multicast) ? causal_head_group(H_q, H_kv, N_k, d, B * H_q) : 1;
 
   FwdMaps maps{};
   maps.k = tk;

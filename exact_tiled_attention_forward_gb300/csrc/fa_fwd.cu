@@ -297,6 +297,29 @@ __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t s
   }
 }
 
+// Query block number qlin -> (b * H_q + h, query block). Non-causal: head-major,
+// blocks in order. Causal: blocks differ in length, and the grid is handed
+// out in order, so the heads are taken in groups of p.hgroup (as many as keep
+// their K/V in L2 together); inside a group the blocks run longest first with
+// the group's heads interleaved (the last block of every head, then the one
+// before, ...). Head-major order would leave the longest blocks of the last
+// heads to start at the very end. hgroup = 1 is head-major, longest first.
+__device__ __forceinline__ void block_of(const FwdParams& p, int qlin, int& bh, int& qb) {
+  if (!p.causal) {
+    bh = qlin / p.n_qb;
+    qb = qlin - bh * p.n_qb;
+    return;
+  }
+  const int g = p.hgroup;
+  const int per = g * p.n_qb;
+  const int grp = qlin / per;
+  const int w = qlin - grp * per;
+  const int gh = min_i(g, p.n_bh - grp * g);   // heads in this group (the last may have fewer)
+  const int rank = w / gh;
+  bh = grp * g + (w - rank * gh);
+  qb = p.n_qb - 1 - rank;
+}
+
 // Query block and key-tile counts of work unit u (see the kernel's unit comment).
 struct UnitInfo {
   int bh, qb, split, S, slot, lo, n0, n1, nmax;
@@ -310,9 +333,7 @@ __device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int u) {
     const int v = u - p.u_full;
     qlin = p.u_full + v / p.s_tail; ui.split = v % p.s_tail; ui.S = p.s_tail; ui.slot = v;
   }
-  const int qr = qlin % p.n_qb;
-  ui.bh = qlin / p.n_qb;
-  ui.qb = p.causal ? (p.n_qb - 1 - qr) : qr;
+  block_of(p, qlin, ui.bh, ui.qb);
   const int q0 = ui.qb * kBlockRows;
   // key tiles each query tile needs: [0, kv_hi); fully masked tiles are never visited
   int kvh[2];
@@ -388,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the rest split the last query blocks' key ranges into s_tail parts whose
   // partial (m, l, O) go to the workspace (merged by fa_merge_kernel). Query
   // blocks are numbered head-major (a head's blocks are adjacent, so its K/V
-  // stay in L2); causal blocks run longest first within a head.
+  // stay in L2); causal blocks run longest first within groups of heads whose
+  // K/V fit in L2 together (block_of).
   const int u = blockIdx.x;
   const bool idle = MC && u >= p.n_units;   // completes the last cluster only
   const UnitInfo ui = unit_info(p, idle ? 0 : u);
@@ -817,10 +839,8 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   const int t = (int)(wrow / kBlockRows);
   const int r = (int)(wrow % kBlockRows);
   if (t >= p.n_tail) return;
-  const int qlin = p.u_full + t;
-  const int bh = qlin / p.n_qb;
-  const int qr = qlin % p.n_qb;
-  const int qb = p.causal ? (p.n_qb - 1 - qr) : qr;
+  int bh, qb;
+  block_of(p, p.u_full + t, bh, qb);
   const int row = qb * kBlockRows + r;
   if (row >= p.N_q) return;
   const int S = p.s_tail;

@@ -19,6 +19,8 @@ struct FwdParams {
   int causal;
   int kv_off;       // N_k - N_q: query i sees key j iff j <= i + kv_off (causal)
   int n_qb;         // query blocks of kBlockRows rows per (b, h)
+  int n_bh;         // B * H_q
+  int hgroup;       // causal block order: heads per group (>= 1; 1 = head-major)
   int n_kv_tiles;   // ceil(N_k / kTileN)
   int u_full;       // units [0, u_full) are whole query blocks (query blocks 0 .. u_full-1)
   int n_tail;       // query blocks u_full .. u_full+n_tail-1 are split ...

@@ -127,6 +127,28 @@ def test_split_merge_modes(fa, shape, cluster_merge, monkeypatch):
     compare(o, lse, *run_oracle(a))
 
 
+CAUSAL_GROUPS = [
+    (2, 8, 2, 2560, 2560, 64, True),     # 160 whole blocks (more than a wave), GQA 4
+    (1, 10, 5, 2048, 2048, 128, True),   # 80 blocks: split key ranges, merged by block number
+    (1, 6, 6, 1500, 3000, 128, True),    # N_q < N_k, ragged last block
+]
+
+
+@pytest.mark.parametrize("group", [None, "1", "3"], ids=["default", "g1", "g3"])
+@pytest.mark.parametrize("shape", CAUSAL_GROUPS, ids=lambda s: "x".join(map(str, s[:6])))
+def test_causal_head_groups(fa, shape, group, monkeypatch):
+    # causal blocks run longest first across groups of heads; groups of 3 leave a
+    # short last group, and every block must still be written exactly once
+    if group is None:
+        monkeypatch.delenv("FA_CAUSAL_HEAD_GROUP", raising=False)
+    else:
+        monkeypatch.setenv("FA_CAUSAL_HEAD_GROUP", group)
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=9, k_row_frac=0.01)
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
+
+
 def test_tiny_workload_n256_d64(fa):
     a = I.make_workload("tiny_n256_d64")
     o, lse = _run(fa, a)
