@@ -197,6 +197,18 @@ class ClockSampler:
                 "source": src}
 
 
+def to_device(torch, x, dev):
+    """An input array on the device: FP16 values as torch.float16, BF16 bit
+    patterns as torch.bfloat16."""
+    if x.dtype == np.float16:
+        return torch.from_numpy(x).to(dev)
+    return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def elem_dtype(torch, a):
+    return torch.float16 if a.dtype == "f16" else torch.bfloat16
+
+
 def workload_config(name: str):
     cfg = dict(I.WORKLOADS[name])
     a_flops = W.flops_pages(cfg["B"], cfg["H_q"], cfg["N_q"], cfg["N_k"], cfg["d"], cfg["causal"])
@@ -244,18 +256,18 @@ def fused_launches_per_step(fa, cfg) -> int:
                               cfg["causal"])["launches"]
 
 
-def time_decode(fa, torch, dev, flush, stream, steps, warmup, world):
+def time_decode(fa, torch, dev, flush, stream, steps, warmup, world, dtype="bf16"):
     """Device time of the decode workload; GB/s of algorithmic bytes (K, V once
     per KV head, Q read, O and LSE written). Two input sets used in turn (each
     537 MB, several times L2), steps back to back between two events; also the
     same steps one at a time with L2 flushed before each ("flushed")."""
     cfg, _, a_bytes, _ = workload_config(DECODE_WORKLOAD)
-    a = I.make_workload(DECODE_WORKLOAD)
-    to = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    a = I.make_workload(DECODE_WORKLOAD, dtype=dtype)
+    to = lambda x: to_device(torch, x, dev)
     B, Hq, Hkv, Nq, Nk, d = a.shape_args
     q, k, v = to(a.q), to(a.k), to(a.v)
     sets = [(q, k, v), (q.clone(), k.clone(), v.clone())]
-    o = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((B, Hq, Nq, d), dtype=elem_dtype(torch, a), device=dev)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
 
     def step(i):
@@ -294,8 +306,8 @@ def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_
     one stream with nothing overlapped)."""
     B, Hq, Hkv, Nq, Nk, d = a.shape_args
     nq, nk = a.q.size, a.k.size
-    hin = torch.from_numpy(np.concatenate([a.q.reshape(-1), a.k.reshape(-1), a.v.reshape(-1)])
-                           .view(np.int16)).view(torch.bfloat16).pin_memory()
+    hin = to_device(torch, np.concatenate([a.q.reshape(-1), a.k.reshape(-1), a.v.reshape(-1)]),
+                    "cpu").pin_memory()
     o_bytes, l_bytes = B * Hq * Nq * d * 2, B * Hq * Nq * 4
     din = [torch.empty_like(hin, device=dev) for _ in range(2)]
     dout = [torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
@@ -304,7 +316,7 @@ def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_
     for x, y in zip(din, dout):
         slots.append((x[:nq].view(B, Hq, Nq, d), x[nq:nq + nk].view(B, Hkv, Nk, d),
                       x[nq + nk:].view(B, Hkv, Nk, d),
-                      y[:o_bytes].view(torch.bfloat16).view(B, Hq, Nq, d),
+                      y[:o_bytes].view(elem_dtype(torch, a)).view(B, Hq, Nq, d),
                       y[o_bytes:].view(torch.float32).view(B, Hq, Nq)))
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
@@ -378,12 +390,16 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fused", choices=["fused", "naive", "reference"])
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="element type of Q, K, V and O (the unfused baseline is BF16 only)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=500,
                     help="timed steps of the decode workload reported beside the prefill line")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of host time for the cpu_baseline leg (0 disables it)")
     args = ap.parse_args()
+    if args.impl == "naive" and args.dtype != "bf16":
+        ap.error("the unfused baseline is BF16 only")
     warmup = max(3, args.warmup)
 
     rank, world, local = R.replica_env()
@@ -395,7 +411,7 @@ def main():
         # The oracle on the host cores, rank 0 only; other ranks exit without work.
         if rank != 0:
             return
-        a = I.make_workload(args.workload)
+        a = I.make_workload(args.workload, dtype=args.dtype)
         B, Hq = cfg["B"], cfg["H_q"]
         # a bounded sample per step: about 40 s of oracle time over the whole run
         rows_sample = max(16, min(B * Hq * cfg["N_q"], 2048, (2048 * 200) // max(1, args.steps)))
@@ -432,13 +448,13 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     fa.lib()
 
-    a = I.make_workload(args.workload)
+    a = I.make_workload(args.workload, dtype=args.dtype)
     B, Hq, Hkv, Nq, Nk, d = a.shape_args
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
 
     def to_dev(x):
-        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+        return to_device(torch, x, dev)
 
     q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
     fn = fa.fa_forward if args.impl == "fused" else fa.fa_naive_forward
@@ -454,7 +470,7 @@ def main():
     n_sets = min(4096, max(2, -(-2 * l2_bytes // set_bytes)))
     # one copy kernel per input: [n_sets, ...] tensors whose slices are the sets
     qs, ks, vs = (x.unsqueeze(0).expand(n_sets, *x.shape).contiguous() for x in (q, k, v))
-    sets = [(qs[i], ks[i], vs[i], torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev),
+    sets = [(qs[i], ks[i], vs[i], torch.empty((B, Hq, Nq, d), dtype=elem_dtype(torch, a), device=dev),
              torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)) for i in range(n_sets)]
     del q, k, v
 
@@ -531,7 +547,8 @@ def main():
     # ---- secondary half of the metric: decode HBM GB/s (batch 16, 32/8 heads, 8192 keys)
     decode = None
     if args.impl == "fused" and not decode_cfg and args.decode_steps > 0:
-        decode = time_decode(fa, torch, dev, flush, stream, args.decode_steps, warmup, world)
+        decode = time_decode(fa, torch, dev, flush, stream, args.decode_steps, warmup, world,
+                             args.dtype)
 
     if rank != 0:
         torch.distributed.destroy_process_group()
@@ -548,7 +565,9 @@ def main():
         roof = {"bound": "tensor", "unit": "TFLOP/s"}
     traffic = profiled_traffic(args.workload) if args.impl == "fused" else None
     roof.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
-                 "traffic": traffic, "peak_source": f"{peak_src} (burst)",
+                 "traffic": traffic,
+                 "peak_source": (f"{peak_src} (burst)" if args.dtype == "bf16" or decode_cfg else
+                                 f"{peak_src} BF16 burst x nominal FP16/BF16 ratio 1 (2.25 PF both)"),
                  "algorithmic_per_launch": a_bytes if decode_cfg else a_flops,
                  "kernel": "fa_fwd_kernel" if args.impl == "fused" else "naive (3 kernels)"})
 
@@ -563,7 +582,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "impl": args.impl,
         "config": {"workload": args.workload, **{k2: cfg[k2] for k2 in
                    ("B", "H_q", "H_kv", "N_q", "N_k", "d", "causal")},

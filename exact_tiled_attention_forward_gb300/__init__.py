@@ -9,8 +9,9 @@ missing or fails to load, every call raises.
     import exact_tiled_attention_forward_gb300 as fa
     o, lse = fa.fa_forward(q, k, v, causal=False)          # torch CUDA tensors
 
-Tensors: q ``[B, H_q, N_q, d]``, k/v ``[B, H_kv, N_k, d]`` BF16 contiguous;
-returns o ``[B, H_q, N_q, d]`` BF16 and lse ``[B, H_q, N_q]`` FP32.
+Tensors: q ``[B, H_q, N_q, d]``, k/v ``[B, H_kv, N_k, d]`` BF16 (or FP16, through
+``fa_forward_fp16``) contiguous; returns o ``[B, H_q, N_q, d]`` of the same type
+and lse ``[B, H_q, N_q]`` FP32.
 """
 from __future__ import annotations
 
@@ -47,6 +48,7 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 
 _SIGNATURES = {
     "fa_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_forward_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
@@ -107,10 +109,25 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
 
 
+def _check_dtypes(dtype, q, k, v, out, lse):
+    """All of q, k, v, out in `dtype`, lse FP32 (or None): libfa reads raw memory."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t is not None and t.dtype != dtype:
+            raise TypeError(f"{name} is {t.dtype}, expected {dtype}")
+    if lse is not None and lse.dtype != torch.float32:
+        raise TypeError(f"lse is {lse.dtype}, expected torch.float32")
+
+
 def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
                return_lse: bool = True, stream=None):
-    """Fused forward on the current CUDA stream. Returns ``(o, lse)``."""
+    """Fused forward on the current CUDA stream. Returns ``(o, lse)``.
+    BF16 tensors; FP16 tensors are passed on to ``fa_forward_fp16``."""
     import torch
+    if q.dtype == torch.float16:
+        return fa_forward_fp16(q, k, v, causal=causal, scale=scale, out=out, lse=lse,
+                               return_lse=return_lse, stream=stream)
+    _check_dtypes(torch.bfloat16, q, k, v, out, lse)
     B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -124,12 +141,31 @@ def fa_forward(q, k, v, causal: bool = False, scale: float | None = None, out=No
     return out, lse
 
 
+def fa_forward_fp16(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                    return_lse: bool = True, stream=None):
+    """Fused forward on FP16 q, k, v (FP16 o, FP32 lse). Returns ``(o, lse)``."""
+    import torch
+    _check_dtypes(torch.float16, q, k, v, out, lse)
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.float16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    st = lib().fa_forward_fp16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q,
+                               N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "fa_forward_fp16")
+    return out, lse
+
+
 def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                        lse=None, return_lse: bool = True, stream=None):
     """``fa_forward`` that allocates no device memory inside libfa: split
     partials use libfa's fixed 32 MiB device array (see ``include/fa.h``).
     Concurrent calls race on that array; keep them on one stream. Returns ``(o, lse)``."""
     import torch
+    _check_dtypes(torch.bfloat16, q, k, v, out, lse)
     B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -161,8 +197,9 @@ def fa_naive_workspace_bytes(B: int, H_q: int, N_q: int, N_k: int) -> int:
 
 def fa_naive_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                      lse=None, workspace=None, return_lse: bool = True, stream=None):
-    """Unfused three-kernel baseline. Returns ``(o, lse)``."""
+    """Unfused three-kernel baseline (BF16). Returns ``(o, lse)``."""
     import torch
+    _check_dtypes(torch.bfloat16, q, k, v, out, lse)
     B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)

@@ -325,7 +325,8 @@ FwdPlan prefill_plan(int B, int H_q, int N_q, int N_k, int d, int causal) {
 
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t strm,
-                 const WorkspaceSource& wsrc) {
+                 const WorkspaceSource& wsrc, int elem) {
+  if (elem != 0 && elem != 1) return FA_ERR_INVALID_ARG;
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
   int st = validate(q, k, v, o, lse, s, scale);
   if (st != FA_OK) return st;
@@ -353,7 +354,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     p.n_parts = dp.n_parts;
     p.cm = dp.cm;
     p.c = scale * 1.4426950408889634f;
-    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.q = static_cast<const uint16_t*>(q);
+    p.elem = elem;
     p.o = o;
     p.lse = lse;
     p.status = status;
@@ -390,7 +392,9 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.s_tail = pl.s_tail;
   p.n_units = (int)pl.units;
   p.cm = pl.cluster_merge;
-  const bool multicast = pl.n_tail == 0 && pl.units >= 2 && multicast_enabled();
+  // (the multicast variant is built for BF16 only)
+  const bool multicast = pl.n_tail == 0 && pl.units >= 2 && elem == 0 && multicast_enabled();
+  p.elem = elem;
   p.n_bh = B * H_q;
   // the multicast variant pairs adjacent blocks of one head: head-major there
   p.hgroup = (causal && !multicast) ? causal_head_group(H_q, H_kv, N_k, d, B * H_q) : 1;
@@ -508,6 +512,12 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream) {
   return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
                       static_cast<cudaStream_t>(stream), pool_workspace());
+}
+
+int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream) {
+  return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
+                      static_cast<cudaStream_t>(stream), pool_workspace(), 1);
 }
 
 int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,

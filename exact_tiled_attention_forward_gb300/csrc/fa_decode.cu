@@ -54,13 +54,22 @@ struct DecCfg {
   static_assert(4 * 16 * D * 4 <= kTileBytes, "merge buffer must fit in the K tile");
 };
 
+// D (16 x 8, FP32) += A (16 x 16) B (16 x 8), A and B both BF16 or both FP16.
+template <Elem E>
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (E == Elem::F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -84,7 +93,7 @@ __device__ __forceinline__ uint32_t sw128_addr(uint32_t base, int key, int ch16)
   return base + (uint32_t)(box * (kDecKeys * 128) + key * 128 + ((ch ^ (key & 7)) << 4));
 }
 
-template <int D>
+template <int D, Elem E>
 __global__ void __launch_bounds__(kDecThreads)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecParams p) {
@@ -176,8 +185,8 @@ __global__ void __launch_bounds__(kDecThreads)
           const int key = kw + 16 * np + 8 * (i >> 1) + rr;
           uint32_t b00, b01, b10, b11;
           ldsm_x4(sw128_addr(sb + C::kOffK, key, 2 * ks + (i & 1)), b00, b01, b10, b11);
-          mma16816(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-          mma16816(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+          mma16816<E>(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
+          mma16816<E>(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
         }
       }
     }
@@ -235,10 +244,10 @@ __global__ void __launch_bounds__(kDecThreads)
     uint32_t pa[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      pa[j][0] = pack_bf16x2(sacc[2 * j][0], sacc[2 * j][1]);
-      pa[j][1] = pack_bf16x2(sacc[2 * j][2], sacc[2 * j][3]);
-      pa[j][2] = pack_bf16x2(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
-      pa[j][3] = pack_bf16x2(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+      pa[j][0] = pack2<E>(sacc[2 * j][0], sacc[2 * j][1]);
+      pa[j][1] = pack2<E>(sacc[2 * j][2], sacc[2 * j][3]);
+      pa[j][2] = pack2<E>(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
+      pa[j][3] = pack2<E>(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
     }
     // ---- O += P V: D/8 n-tiles of 8 columns
     const bool okV = mbar_wait(barV, ph, &abort_flag, p.status);
@@ -251,8 +260,8 @@ __global__ void __launch_bounds__(kDecThreads)
           const int key = kw + 16 * j + 8 * (i & 1) + rr;
           uint32_t b00, b01, b10, b11;
           ldsm_x4_t(sw128_addr(sb + C::kOffV, key, 2 * dp + (i >> 1)), b00, b01, b10, b11);
-          mma16816(oacc[2 * dp], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b00, b01);
-          mma16816(oacc[2 * dp + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b10, b11);
+          mma16816<E>(oacc[2 * dp], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b00, b01);
+          mma16816<E>(oacc[2 * dp + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b10, b11);
         }
       }
     }
@@ -380,9 +389,9 @@ __global__ void __launch_bounds__(kDecThreads)
       const int hq = hk * p.G + hl;
       const size_t orow = ((size_t)b * p.H_q + hq) * p.N_q + i;
       uint2 o2;
-      o2.x = pack_bf16x2(acc.x, acc.y);
-      o2.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow * D + dcol) = o2;
+      o2.x = pack2<E>(acc.x, acc.y);
+      o2.y = pack2<E>(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.o) + orow * D + dcol) = o2;
       if (dcol == 0 && p.lse) {
         const float L = sML[2 * m + 1];
         p.lse[orow] = L > 0.f ? (sML[2 * m] + __log2f(L)) * kLn2d : -INFINITY;
@@ -398,7 +407,7 @@ __global__ void __launch_bounds__(kDecThreads)
 // column t over the chunks with independent, coalesced loads.
 constexpr int kMergeMaxChunks = 1024;   // chunks merged per pass (longer rows loop)
 
-template <int D>
+template <int D, Elem E>
 __global__ void __launch_bounds__(D) fa_decode_merge_kernel(const DecParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float s_w[kMergeMaxChunks];
@@ -467,22 +476,24 @@ __global__ void __launch_bounds__(D) fa_decode_merge_kernel(const DecParams p) {
   __syncthreads();
   const float L = s_ML[1];
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)b * p.H_q + hq) * p.N_q + i) * D;
-  orow[tid] = __float2bfloat16_rn(acc * inv);
+  uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)b * p.H_q + hq) * p.N_q + i) * D;
+  orow[tid] = (uint16_t)(pack2<E>(acc * inv, 0.f) & 0xFFFFu);
   if (tid == 0 && p.lse)
     p.lse[((size_t)b * p.H_q + hq) * p.N_q + i] = L > 0.f ? (M + __log2f(L)) * kLn2d : -INFINITY;
 }
 
-template <int D>
+template <int D, Elem E>
 cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
                             cudaStream_t stream) {
   using C = DecCfg<D>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool attr[64] = {false};   // per device; a repeated set is harmless
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr[dev] = true;
   }
   const long long ctas = (long long)p.B * p.H_kv * p.n_parts;
   cudaError_t e;
@@ -500,9 +511,9 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
     ka[0].val.clusterDim.z = 1;
     kc.attrs = ka;
     kc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&kc, fa_decode_kernel<D>, tk, tv, p);
+    e = cudaLaunchKernelEx(&kc, fa_decode_kernel<D, E>, tk, tv, p);
   } else {
-    fa_decode_kernel<D><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
+    fa_decode_kernel<D, E><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || p.cm) return e;
@@ -516,7 +527,7 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_decode_merge_kernel<D>, p);
+  return cudaLaunchKernelEx(&cfg, fa_decode_merge_kernel<D, E>, p);
 }
 
 }  // namespace
@@ -525,10 +536,11 @@ size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d) {
   return (size_t)B * H_kv * n_parts * R * ((size_t)d * 4 + 8);
 }
 
+// (the FP16 kernel has the same resources: one answer serves both)
 template <int D>
 int decode_cluster_capacity_t(int parts) {
   using C = DecCfg<D>;
-  if (cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fa_decode_kernel<D, Elem::BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -545,7 +557,7 @@ int decode_cluster_capacity_t(int parts) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fa_decode_kernel<D>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, fa_decode_kernel<D, Elem::BF16>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -591,7 +603,11 @@ DecPlan decode_plan(long long heads, int n_chunks, int d, int sms, bool cluster_
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
                           cudaStream_t stream) {
   if ((long long)p.B * p.H_kv * p.n_parts <= 0) return cudaSuccess;
-  return d == 128 ? launch_decode_t<128>(tk, tv, p, stream) : launch_decode_t<64>(tk, tv, p, stream);
+  if (p.elem == (int)Elem::F16)
+    return d == 128 ? launch_decode_t<128, Elem::F16>(tk, tv, p, stream)
+                    : launch_decode_t<64, Elem::F16>(tk, tv, p, stream);
+  return d == 128 ? launch_decode_t<128, Elem::BF16>(tk, tv, p, stream)
+                  : launch_decode_t<64, Elem::BF16>(tk, tv, p, stream);
 }
 
 }  // namespace fa

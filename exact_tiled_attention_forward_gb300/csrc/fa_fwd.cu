@@ -37,11 +37,15 @@
 // Softmax per tile: exponentials are computed against the row's reference
 // max m (log2 units). A row's reference is set from the tile max on its first
 // live tile; afterwards P = 2^(s c - m) may exceed 1, and only when the first
-// half's sum of P exceeds 2^16 (so some P may) or the second half's max exceeds
-// m + 16 is the reference raised to the tile max, O and l rescaled and the
-// first half redone, all before P is handed over. P <= 2^16 keeps every value
-// in range, and the final O / l and LSE are exact because O and l share the
+// half's sum of P exceeds 2^tau (so some P may) or the second half's max exceeds
+// m + tau is the reference raised to the tile max, O and l rescaled and the
+// first half redone, all before P is handed over. tau = 16 for BF16 and 15 for
+// FP16 tensors: P <= 2^tau keeps every value in range of the element type P is
+// stored in, and the final O / l and LSE are exact because O and l share the
 // reference. An overflowed P makes the sum infinite and takes the same path.
+//
+// Element type: BF16 or FP16 (Q, K, V, P and O all of one type, FP32 accumulation);
+// only the instruction descriptors, the conversions and tau differ.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -56,8 +60,13 @@ constexpr int kRegsSoftmax = 216;   // per thread, warpgroups 0-1
 constexpr int kRegsOther = 72;      // per thread, warpgroup 2
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
-constexpr float kTau = 16.0f;          // a reference may lag the row max by this much (log2)
-constexpr float kSumCap = 65536.0f;    // 2^kTau
+// A row's reference max may lag its true max by up to kTau (log2 units), so P
+// stays <= 2^kTau: 2^16 in BF16, 2^15 in FP16 (whose largest finite value is 65504).
+template <Elem E>
+struct Lag {
+  static constexpr float kTau = E == Elem::F16 ? 15.0f : 16.0f;
+  static constexpr float kSumCap = E == Elem::F16 ? 32768.0f : 65536.0f;   // 2^kTau
+};
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -101,6 +110,7 @@ __device__ __forceinline__ int max_i(int a, int b) { return a > b ? a : b; }
 // the sum of P (FP32). Software-pipelined in chunks of 16: the exponentials of
 // chunk k+1 are issued before chunk k is packed and stored, so the exp unit
 // stays busy.
+template <Elem E>
 __device__ __forceinline__ float exp_half(const float* s, float c, float mb, uint32_t tP) {
   float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
   float pa[16], pb[16];
@@ -122,7 +132,7 @@ __device__ __forceinline__ float exp_half(const float* s, float c, float mb, uin
     }
     uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(pa[2 * i], pa[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) pk[i] = pack2<E>(pa[2 * i], pa[2 * i + 1]);
     tmem_st8(tP + (uint32_t)k * 8u, pk);
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
@@ -222,7 +232,7 @@ __device__ __forceinline__ void cm_send(uint32_t sb, uint32_t ml_base, int S, in
 // written by TMA stores (tmO has R-row boxes). S (2, 4 or 8) is a template
 // parameter so the per-source arrays are exactly sized. Not inlined: it runs
 // once per CTA, and compiled apart it leaves the main loop's registers alone.
-template <int D, int S>
+template <int D, int S, Elem E>
 __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t stage, int w, int warp,
                                        int lane, bool ok, const FwdParams& p, const CUtensorMap* tmO,
                                        int bh, int q0) {
@@ -282,8 +292,8 @@ __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t s
       }
       const int bx = cb >> 3, cbb = cb & 7;
       st_shared_v4(stage + (uint32_t)(bx * R + lr) * 128u + ((uint32_t)(cbb ^ (lr & 7)) << 4),
-                   pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                   pack_bf16x2(acc[6], acc[7]));
+                   pack2<E>(acc[0], acc[1]), pack2<E>(acc[2], acc[3]), pack2<E>(acc[4], acc[5]),
+                   pack2<E>(acc[6], acc[7]));
     }
   }
   fence_proxy_async_smem();
@@ -367,7 +377,7 @@ __device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int u) {
 // causal pair walks the union of its key ranges (the shorter unit only
 // releases the extra tiles). Single-GPU only: the tiles come from this GPU's
 // own memory.
-template <int D, bool MC>
+template <int D, bool MC, Elem E>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -551,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (share) mma_commit_mc_w(bar(C::kBarEmpty + st), (uint16_t)0x3);
           else mma_commit_w(bar(C::kBarEmpty + st));
         };
-        constexpr uint32_t idS = idesc_bf16_f32(128, kTileN, false);
-        constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+        constexpr uint32_t idS = idesc_f32(128, kTileN, false, E);
+        constexpr uint32_t idO = idesc_f32(128, D, true, E);
         // Descriptors are built once; each MMA adds a compile-time offset to the
         // start-address field (16-byte units) of the low word, so issuing stays
         // ahead of the tensor core.
@@ -676,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!spec) {
         // some row's first live tile: references from the tile max
         const float m_tile = max_scores<kTileN>(s) * c;
-        const bool need = m_tile > m_ref + kTau;   // always, for a row without a reference
+        const bool need = m_tile > m_ref + Lag<E>::kTau;   // always, for a row without a reference
         if (__any_sync(0xffffffffu, need)) {
           float alpha = 1.f;
           if (need) {
@@ -687,17 +697,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0) rescale_o<D>(tO, alpha);   // O_X holds PV_X(0..j-1), stable (S_X(j) commit)
         }
         const float mb = m_ref == -INFINITY ? 0.f : m_ref;
-        const float r1 = exp_half(s, c, mb, tS);
+        const float r1 = exp_half<E>(s, c, mb, tS);
         publish(bar(C::kBarP1 + X));
-        const float r2 = exp_half(s + 64, c, mb, tS + 32);
+        const float r2 = exp_half<E>(s + 64, c, mb, tS + 32);
         publish(bar(C::kBarP2 + X));
         l += r1 + r2;
       } else {
         // the first half's P against the reference, and the second half's max:
         // any rescale is decided here, while O_X is stable (S_X(j) commit)
-        float r1 = exp_half(s, c, m_ref, tS);
+        float r1 = exp_half<E>(s, c, m_ref, tS);
         const float m2 = max_scores<kTileN / 2>(s + 64) * c;
-        const bool need = !(r1 <= kSumCap) || m2 > m_ref + kTau;
+        const bool need = !(r1 <= Lag<E>::kSumCap) || m2 > m_ref + Lag<E>::kTau;
         if (__any_sync(0xffffffffu, need)) {
           float alpha = 1.f;
           if (need) {
@@ -707,11 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
           }
           rescale_o<D>(tO, alpha);
-          r1 = exp_half(s, c, m_ref, tS);
+          r1 = exp_half<E>(s, c, m_ref, tS);
         }
         publish(bar(C::kBarP1 + X));
         // the second half's P <= 2^kTau now
-        const float r2 = exp_half(s + 64, c, m_ref, tS + 32);
+        const float r2 = exp_half<E>(s + 64, c, m_ref, tS + 32);
         publish(bar(C::kBarP2 + X));
         l += r1 + r2;
       }
@@ -732,9 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       cluster_sync();   // all partials of this CTA's rows have landed
       {
         const uint32_t rb = sb + C::kOffQ, mb2 = sb + C::kOffCm, stg = sb + C::kOffQ + C::kCmStage;
-        if (p.s_tail == 2) cm_reduce<D, 2>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
-        else if (p.s_tail == 4) cm_reduce<D, 4>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
-        else cm_reduce<D, 8>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        if (p.s_tail == 2) cm_reduce<D, 2, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        else if (p.s_tail == 4) cm_reduce<D, 4, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        else cm_reduce<D, 8, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
       }
     } else if (slot < 0) {
       // ---- final epilogue: O / l -> BF16 into this tile's Q slot (128-byte
@@ -757,10 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < 4; ++g) {
             const uint32_t ch = (uint32_t)(((cc & 63) >> 3) + g);   // 16-byte chunk in the row
             st_shared_v4(rowaddr + ((ch ^ (uint32_t)(r & 7)) << 4),
-                         pack_bf16x2(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
-                         pack_bf16x2(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
-                         pack_bf16x2(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
-                         pack_bf16x2(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
+                         pack2<E>(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
+                         pack2<E>(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
+                         pack2<E>(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
+                         pack2<E>(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
           }
         }
         if (valid_row && p.lse)
@@ -830,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // O_s / L, LSE = (M + log2 L) ln 2. One warp per row, lanes across columns.
 // Launched as a programmatic dependent of fa_fwd_kernel: it may be resident
 // early and waits (griddepcontrol.wait) until that grid has completed.
-template <int D>
+template <int D, Elem E>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kCols = D / 32;  // columns per lane
@@ -890,32 +900,34 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
       acc[3] += ws * va[s2].w;
     }
   }
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N_q + row) * D;
+  uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)bh * p.N_q + row) * D;   // 16-bit elements
   if constexpr (kCols == 4) {
     uint2 v;
-    v.x = pack_bf16x2(acc[0], acc[1]);
-    v.y = pack_bf16x2(acc[2], acc[3]);
+    v.x = pack2<E>(acc[0], acc[1]);
+    v.y = pack2<E>(acc[2], acc[3]);
     *reinterpret_cast<uint2*>(orow + lane * 4) = v;
   } else {
-    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack_bf16x2(acc[0], acc[1]);
+    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack2<E>(acc[0], acc[1]);
   }
   if (lane == 0 && p.lse) p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
-// Opt in to the kernel's dynamic shared memory (once per process and device set-up).
-template <int D, bool MC>
+// Opt in to the kernel's dynamic shared memory (once per device and kernel).
+template <int D, bool MC, Elem E>
 cudaError_t ensure_smem_attr() {
-  static bool attr = false;  // benign race: setting the attribute twice is harmless
-  if (attr) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool attr[64] = {false};  // benign race: setting the attribute twice is harmless
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (attr[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<D>::kSmemBytes);
-  if (e == cudaSuccess) attr = true;
+  if (e == cudaSuccess) attr[dev] = true;
   return e;
 }
 
 template <int D>
 int cluster_capacity_t(int s) {
-  if (ensure_smem_attr<D, false>() != cudaSuccess) return 0;
+  if (ensure_smem_attr<D, false, Elem::BF16>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)s);
   cfg.blockDim = dim3(kThreads);
@@ -928,16 +940,17 @@ int cluster_capacity_t(int s) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fa_fwd_kernel<D, false>, &cfg) != cudaSuccess) {
+  // the FP16 kernel has the same resources: one answer serves both
+  if (cudaOccupancyMaxActiveClusters(&n, fa_fwd_kernel<D, false, Elem::BF16>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <int D, bool MC>
+template <int D, bool MC, Elem E>
 cudaError_t launch_main_t(const FwdMaps& m, const FwdParams& p, int units, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<D, MC>();
+  cudaError_t e = ensure_smem_attr<D, MC, E>();
   if (e != cudaSuccess) return e;
   // programmatic launch: set-up may overlap the previous kernel on the stream
   // (the kernel waits for it before its first global read and write)
@@ -955,14 +968,18 @@ cudaError_t launch_main_t(const FwdMaps& m, const FwdParams& p, int units, cudaS
   at[1].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = (MC || p.cm) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, MC>, m.q, m.k, m.v, m.o, m.part, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, MC, E>, m.q, m.k, m.v, m.o, m.part, p);
 }
 
-template <int D>
+// multicast exists for BF16 only (the caller never asks for it with FP16)
+template <int D, Elem E>
 cudaError_t launch_fwd_t(const FwdMaps& m, const FwdParams& p, int units, bool multicast,
                          cudaStream_t stream) {
-  cudaError_t e = multicast ? launch_main_t<D, true>(m, p, units, stream)
-                            : launch_main_t<D, false>(m, p, units, stream);
+  cudaError_t e;
+  if constexpr (E == Elem::BF16)
+    e = multicast ? launch_main_t<D, true, E>(m, p, units, stream) : launch_main_t<D, false, E>(m, p, units, stream);
+  else
+    e = multicast ? cudaErrorInvalidValue : launch_main_t<D, false, E>(m, p, units, stream);
   if (e != cudaSuccess || p.n_tail == 0 || p.cm) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(((long long)p.n_tail * kBlockRows + 7) / 8));
@@ -974,7 +991,7 @@ cudaError_t launch_fwd_t(const FwdMaps& m, const FwdParams& p, int units, bool m
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_merge_kernel<D>, p);
+  return cudaLaunchKernelEx(&cfg, fa_merge_kernel<D, E>, p);
 }
 
 }  // namespace
@@ -996,8 +1013,11 @@ size_t fwd_smem_bytes(int d) {
 cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, bool multicast,
                        cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  return d == 128 ? launch_fwd_t<128>(m, p, units, multicast, stream)
-                  : launch_fwd_t<64>(m, p, units, multicast, stream);
+  if (p.elem == (int)Elem::F16)
+    return d == 128 ? launch_fwd_t<128, Elem::F16>(m, p, units, multicast, stream)
+                    : launch_fwd_t<64, Elem::F16>(m, p, units, multicast, stream);
+  return d == 128 ? launch_fwd_t<128, Elem::BF16>(m, p, units, multicast, stream)
+                  : launch_fwd_t<64, Elem::BF16>(m, p, units, multicast, stream);
 }
 
 }  // namespace fa

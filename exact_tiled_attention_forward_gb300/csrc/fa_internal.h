@@ -27,6 +27,7 @@ struct FwdParams {
   int s_tail;       // ... into s_tail key ranges each (units u_full + t*s_tail + s)
   int n_units;      // work units (the grid may hold one more, idle, CTA to complete a cluster)
   int cm;           // 1: every block is split and its s_tail CTAs (one cluster) merge in-kernel
+  int elem;         // element type of Q, K, V, O: 0 = BF16, 1 = FP16 (host-side dispatch)
   float c;          // scale * log2(e)
   void* o;          // bf16 [B][H_q][N_q][d]
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
@@ -74,8 +75,9 @@ struct DecParams {
   int cpc;           // chunks per CTA (a run of consecutive chunks)
   int n_parts;       // ceil(n_chunks / cpc): CTAs, and partials, per (batch, KV head)
   int cm;            // 1: the n_parts CTAs of a KV head form a cluster and merge in-kernel
+  int elem;          // element type of Q, K, V, O: 0 = BF16, 1 = FP16 (host-side dispatch)
   float c;           // scale * log2(e)
-  const __nv_bfloat16* q;  // [B][H_q][N_q][d]
+  const uint16_t* q;  // [B][H_q][N_q][d], 16-bit elements (BF16 or FP16)
   void* o;
   float* lse;
   float* part_o;     // fp32 [B*H_kv][n_parts][R][d]
@@ -146,9 +148,10 @@ struct WorkspaceSource {
   void (*release)(void* ptr, cudaStream_t stream);
 };
 const WorkspaceSource& pool_workspace();   // library-owned stream-ordered pool
-// The whole fused forward (validation, decode or prefill plan, launches).
+// The whole fused forward (validation, decode or prefill plan, launches);
+// elem: 0 = BF16, 1 = FP16 tensors.
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t stream,
-                 const WorkspaceSource& ws);
+                 const WorkspaceSource& ws, int elem = 0);
 
 }  // namespace fa

@@ -9,6 +9,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #ifndef FA_WAIT_TIMEOUT_NS
 #define FA_WAIT_TIMEOUT_NS 2000000000ull  // 2 s: every wait in a healthy launch ends in microseconds
@@ -430,18 +431,35 @@ __device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_b
   return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
 
-// Instruction descriptor, kind::f16: BF16 x BF16 -> FP32, dense.
-//   bits 4-5 D format (1 = F32), 7-9 A format (1 = BF16), 10-12 B format (1 = BF16),
-//   bit 15 A major (0 = K), bit 16 B major (1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
+// 16-bit element type of Q, K, V, P and O (FP32 accumulation either way).
+enum class Elem : int { BF16 = 0, F16 = 1 };
+
+// Instruction descriptor, kind::f16: 16-bit x 16-bit -> FP32, dense.
+//   bits 4-5 D format (1 = F32), 7-9 A format and 10-12 B format (0 = F16, 1 = BF16;
+//   A and B always the same type here), bit 15 A major (0 = K), bit 16 B major
+//   (1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f32(int M, int N, bool b_mn_major, Elem e = Elem::BF16) {
+  return (1u << 4) | ((e == Elem::BF16 ? 1u : 0u) << 7) | ((e == Elem::BF16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return idesc_f32(M, N, b_mn_major, Elem::BF16);
 }
 
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two FP32 values rounded (to nearest even) to the element type, low half first.
+template <Elem E>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (E == Elem::F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the attention forward: BF16 Q, K, V ~ N(0, 1).
+"""Seeded synthetic inputs for the attention forward: BF16 (or FP16) Q, K, V ~ N(0, 1).
 
 This module is the only code shared by the CUDA path's callers (tests, bench)
 and the FP64 oracle. It holds no attention arithmetic: it only draws numbers.
@@ -11,10 +11,13 @@ Recipe (fixed, so a seed names one input on every machine that runs it):
   finaliser applied to ``key(seed, s) + (i + 1) * GAMMA``.
 * normal deviates: Box-Muller on pairs of 53-bit uniforms, in float64.
 * storage: float64 -> float32 (round to nearest even) -> bfloat16 (round to
-  nearest even), kept as raw ``uint16`` bit patterns.
+  nearest even), kept as raw ``uint16`` bit patterns; or, for FP16 inputs,
+  float64 -> IEEE binary16 (round to nearest even, numpy's conversion), kept as
+  ``numpy.float16`` arrays. The array's dtype tells the two apart.
 * "1% of K rows scaled by 8": for each (batch, kv-head), ``round(0.01 * N_k)``
   rows are picked without replacement (the rows with the smallest draws of a
-  separate stream) and multiplied by 8, which is exact in bfloat16.
+  separate stream) and multiplied by 8, which is exact in bfloat16 and in
+  binary16 (at these magnitudes).
 
 Layouts: Q is ``[B][H_q][N_q][d]``, K and V are ``[B][H_kv][N_k][d]``, all
 contiguous row-major.
@@ -74,6 +77,21 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f64_to_f16(x: np.ndarray) -> np.ndarray:
+    """float64 -> IEEE binary16, round to nearest even (numpy's conversion)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def normal_f16(seed: int, stream: int, shape) -> np.ndarray:
+    """The deviates of ``normal_bf16``'s stream, rounded to binary16 instead."""
+    count = int(np.prod(shape))
+    out = np.empty(count, dtype=np.float16)
+    for lo in range(0, count, 2 * _CHUNK):
+        hi = min(count, lo + 2 * _CHUNK)
+        out[lo:hi] = f64_to_f16(_normal_slice(seed, stream, lo, hi))
+    return out.reshape(shape)
+
+
 def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
     count = int(np.prod(shape))
     out = np.empty(count, dtype=np.uint16)
@@ -117,7 +135,8 @@ def scaled_rows(seed: int, n_bh: int, n_k: int, frac: float) -> np.ndarray:
 
 @dataclasses.dataclass
 class AttentionInputs:
-    """One seeded problem. Arrays hold bfloat16 bit patterns (uint16)."""
+    """One seeded problem. Arrays hold bfloat16 bit patterns (uint16), or
+    binary16 values (numpy.float16) when ``dtype`` is "f16"."""
     q: np.ndarray
     k: np.ndarray
     v: np.ndarray
@@ -129,6 +148,7 @@ class AttentionInputs:
     d: int
     causal: bool
     scale: float
+    dtype: str = "bf16"
 
     @property
     def shape_args(self):
@@ -137,20 +157,27 @@ class AttentionInputs:
 
 def make_inputs(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int, *,
                 causal: bool = False, scale: float | None = None, seed: int = 0,
-                k_row_frac: float = 0.0, k_row_factor: float = 8.0) -> AttentionInputs:
-    """Draw Q, K, V for one configuration (all BF16 ~ N(0, 1))."""
-    q = normal_bf16(seed, STREAM_Q, (B, H_q, N_q, d))
-    k = normal_bf16(seed, STREAM_K, (B, H_kv, N_k, d))
-    v = normal_bf16(seed, STREAM_V, (B, H_kv, N_k, d))
+                k_row_frac: float = 0.0, k_row_factor: float = 8.0,
+                dtype: str = "bf16") -> AttentionInputs:
+    """Draw Q, K, V for one configuration (all ~ N(0, 1); dtype "bf16" or "f16")."""
+    if dtype not in ("bf16", "f16"):
+        raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
+    draw = normal_f16 if dtype == "f16" else normal_bf16
+    q = draw(seed, STREAM_Q, (B, H_q, N_q, d))
+    k = draw(seed, STREAM_K, (B, H_kv, N_k, d))
+    v = draw(seed, STREAM_V, (B, H_kv, N_k, d))
     if k_row_frac > 0.0:
         rows = scaled_rows(seed, B * H_kv, N_k, k_row_frac)
         kf = k.reshape(B * H_kv, N_k, d)
         for bh in range(B * H_kv):
             sel = kf[bh, rows[bh]]
-            kf[bh, rows[bh]] = f64_to_bf16_bits(bf16_bits_to_f32(sel).astype(np.float64) * k_row_factor)
+            if dtype == "f16":
+                kf[bh, rows[bh]] = f64_to_f16(sel.astype(np.float64) * k_row_factor)
+            else:
+                kf[bh, rows[bh]] = f64_to_bf16_bits(bf16_bits_to_f32(sel).astype(np.float64) * k_row_factor)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    return AttentionInputs(q, k, v, B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale))
+    return AttentionInputs(q, k, v, B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale), dtype)
 
 
 # The five workloads the method is measured on (batch, heads, lengths, head dim,
@@ -169,5 +196,5 @@ WORKLOADS = {
 }
 
 
-def make_workload(name: str, seed: int = 0) -> AttentionInputs:
-    return make_inputs(seed=seed, **WORKLOADS[name])
+def make_workload(name: str, seed: int = 0, dtype: str = "bf16") -> AttentionInputs:
+    return make_inputs(seed=seed, dtype=dtype, **WORKLOADS[name])

@@ -80,6 +80,18 @@ typedef enum {
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream);
 
+/* fa_forward on FP16 tensors: q, k, v and o hold IEEE binary16 values instead
+ * of BF16, with the same layouts and every other convention, result and error
+ * code of fa_forward (FP32 accumulation and LSE). The pages size their
+ * tensors in FP16 ("Flash Attention Mechanics", its opening and "Why Standard
+ * Attention Is Memory-Bound"; "Why is standard attention memory-bound...",
+ * Step 1). P is rounded to FP16 before the P V product; a row's exponentials are kept
+ * at most 2^15 against a reference max, so they never overflow FP16. The paired
+ * multicast loads (FA_MULTICAST=1) are BF16-only and are not used here. */
+int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
+                    void* stream);
+
 /* fa_forward without any device-memory allocation. (The pages have no
  * counterpart: this exists for callers, not for the method.)
  * For callers that cannot allocate device memory on this path: a serving loop

@@ -22,6 +22,7 @@ invariants (see the test files for the pin of each function).
 """
 from .attention import (  # noqa: F401
     bf16_to_f64,
+    to_f64,
     attention_reference,
     attention_rows,
     attention_tiled_online,

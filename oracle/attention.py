@@ -41,6 +41,15 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
         np.float32).astype(np.float64)
 
 
+def to_f64(x: np.ndarray) -> np.ndarray:
+    """Exact widening of an input tensor to float64: IEEE binary16 values
+    (numpy.float16 arrays) directly, anything else as bfloat16 bit patterns."""
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        return x.astype(np.float64)
+    return bf16_to_f64(x)
+
+
 def visible_key_count(i: np.ndarray | int, n_q: int, n_k: int, causal: bool):
     """Number of keys query row ``i`` may attend to (keys 0 .. count-1).
 
@@ -89,7 +98,7 @@ def attention_reference(q, k, v, causal: bool = False, scale: float | None = Non
     ``S = scale * Q K^T``, mask, ``P = softmax_row(S)``, ``O = P V`` and
     ``LSE = m + ln l``.
 
-    ``q``: bf16 bits ``[B][H_q][N_q][d]``; ``k``, ``v``: ``[B][H_kv][N_k][d]``.
+    ``q``: bf16 bits (or float16 values) ``[B][H_q][N_q][d]``; ``k``, ``v``: ``[B][H_kv][N_k][d]``.
     Returns ``(O, LSE)`` as float64 arrays ``[B][H_q][N_q][d]``, ``[B][H_q][N_q]``.
     """
     B, H_q, n_q, d = q.shape
@@ -101,10 +110,10 @@ def attention_reference(q, k, v, causal: bool = False, scale: float | None = Non
     lse = np.zeros((B, H_q, n_q))
     for b in range(B):
         for hk in range(H_kv):
-            kh = bf16_to_f64(k[b, hk])
-            vh = bf16_to_f64(v[b, hk])
+            kh = to_f64(k[b, hk])
+            vh = to_f64(v[b, hk])
             for h in range(hk * g, (hk + 1) * g):
-                qh = bf16_to_f64(q[b, h])
+                qh = to_f64(q[b, h])
                 for r0 in range(0, n_q, _ROW_BLOCK):
                     rows = np.arange(r0, min(n_q, r0 + _ROW_BLOCK))
                     o[b, h, rows], lse[b, h, rows] = _head_rows(qh, kh, vh, rows, n_q, n_k,
@@ -125,9 +134,9 @@ def attention_rows(q, k, v, b: int, h: int, rows, causal: bool = False,
         scale = 1.0 / math.sqrt(d)
     hk = h // (H_q // H_kv)
     rows = np.asarray(rows, dtype=np.int64)
-    qh = bf16_to_f64(q[b, h, rows])
-    kh = bf16_to_f64(k[b, hk])
-    vh = bf16_to_f64(v[b, hk])
+    qh = to_f64(q[b, h, rows])
+    kh = to_f64(k[b, hk])
+    vh = to_f64(v[b, hk])
     o = np.zeros((len(rows), d))
     lse = np.zeros(len(rows))
     for r0 in range(0, len(rows), _ROW_BLOCK):
@@ -191,9 +200,9 @@ def attention_tiled_online(q, k, v, block_q: int, block_k: int, causal: bool = F
     lse = np.zeros((B, H_q, n_q))
     for b in range(B):
         for h in range(H_q):
-            qh = bf16_to_f64(q[b, h])
-            kh = bf16_to_f64(k[b, h // g])
-            vh = bf16_to_f64(v[b, h // g])
+            qh = to_f64(q[b, h])
+            kh = to_f64(k[b, h // g])
+            vh = to_f64(v[b, h // g])
             for q0 in range(0, n_q, block_q):
                 q1 = min(q0 + block_q, n_q)
                 rows = np.arange(q0, q1)

@@ -15,16 +15,28 @@ TOL_MAX_ABS_LSE = 1e-3
 # A is the oracle's own definition evaluated on |V|. Each element must satisfy
 #   |dO| <= max(1e-2, TOL_REL_ELEM_O * (A + |O_ref|))   (5e-3 = 1.28 u).
 TOL_REL_ELEM_O = 5e-3
+# The same derivation with FP16's unit roundoff u = 2^-11 (P and O rounded to
+# FP16): 1.28 u = 6.25e-4; the absolute floor (1e-2) stays the stated one.
+TOL_REL_ELEM_O_F16 = 6.25e-4
 
 
-def abs_values(v_bits):
-    """|V| as BF16 bit patterns (sign bit cleared; exact)."""
-    return np.asarray(v_bits, dtype=np.uint16) & np.uint16(0x7FFF)
+def abs_values(v):
+    """|V| in V's own storage (FP16 values, or BF16 bit patterns with the sign
+    bit cleared); exact either way."""
+    v = np.asarray(v)
+    if v.dtype == np.float16:
+        return np.abs(v)
+    return v.astype(np.uint16) & np.uint16(0x7FFF)
 
 
-def to_dev(bits):
+def to_dev(x):
+    """Input array to a CUDA tensor: FP16 values as torch.float16, BF16 bit
+    patterns as torch.bfloat16."""
     import torch
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        return torch.from_numpy(x).cuda()
+    return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
 
 
 def bf16_dev_to_f64(t):
@@ -33,8 +45,9 @@ def bf16_dev_to_f64(t):
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
-            tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE):
-    """Element-wise comparison of O and LSE; returns a dict of error figures."""
+            tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE, elem="bf16"):
+    """Element-wise comparison of O and LSE; returns a dict of error figures.
+    ``elem`` ("bf16" or "f16") picks the element-wise relative bound."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape
@@ -42,7 +55,8 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
     err = np.abs(o_gpu - o_ref)
     max_abs = float(err.max()) if err.size else 0.0
     a_ref = np.abs(o_ref) if o_abs_ref is None else np.asarray(o_abs_ref, dtype=np.float64)
-    bound = np.maximum(tol_o, TOL_REL_ELEM_O * (a_ref + np.abs(o_ref)))
+    rel_elem = TOL_REL_ELEM_O_F16 if elem == "f16" else TOL_REL_ELEM_O
+    bound = np.maximum(tol_o, rel_elem * (a_ref + np.abs(o_ref)))
     worst = float((err / bound).max()) if err.size else 0.0
     denom = float(np.linalg.norm(o_ref))
     rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))

@@ -25,7 +25,7 @@ def lib():
 
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
-    assert set(names) == {"fa_forward", "fa_forward_noalloc", "fa_naive_forward",
+    assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_noalloc", "fa_naive_forward",
                           "fa_naive_workspace_bytes", "fa_forward_plan", "fa_selftest_wait_timeout",
                           "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
                           "fa_version"}
@@ -90,6 +90,15 @@ def test_noalloc_rejects_like_forward(lib):
     assert f(0, 0, 0, 0, 0, 1, 2, 1, 0, 64, 128, 0, 0.1, None) == fa.FA_OK
 
 
+def test_fp16_rejects_like_forward(lib):
+    f = lib.fa_forward_fp16
+    assert f(Q, K, V, O, L, 1, 3, 2, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 96, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q + 8, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert f(0, 0, 0, 0, 0, 1, 2, 1, 0, 64, 128, 0, 0.1, None) == fa.FA_OK
+
+
 def test_empty_query_is_a_no_op(lib):
     # nothing to write: success without touching the device (null pointers allowed)
     assert _fwd(lib, q=0, k=0, v=0, o=0, l=0, Nq=0) == fa.FA_OK
@@ -120,3 +129,24 @@ def test_selftest_rejects_limits_out_of_range(lib):
     # argument checks come before any CUDA call
     assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_selftest_wait_timeout(20_000_000_000, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_checks_element_types():
+    # the binding refuses mixed or unsupported dtypes before anything reaches libfa
+    torch = pytest.importorskip("torch")
+    import exact_tiled_attention_forward_gb300 as fa
+    q16 = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    qb = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    q32 = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        fa.fa_forward(q16, qb, qb)                      # FP16 q, BF16 k and v
+    with pytest.raises(TypeError):
+        fa.fa_forward(qb, qb, qb, out=torch.zeros(1, 1, 8, 64, dtype=torch.float16))
+    with pytest.raises(TypeError):
+        fa.fa_forward(q32, q32, q32)                    # FP32 is not an element type here
+    with pytest.raises(TypeError):
+        fa.fa_forward_fp16(qb, qb, qb)
+    with pytest.raises(TypeError):
+        fa.fa_naive_forward(q16, q16, q16)
+    with pytest.raises(TypeError):
+        fa.fa_forward(qb, qb, qb, lse=torch.zeros(1, 1, 8, dtype=torch.float16))

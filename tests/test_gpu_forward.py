@@ -48,7 +48,8 @@ def _run(fa, a, naive=False):
     import torch
     q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
     B, H_q, H_kv, N_q, N_k, d = a.shape_args
-    ob, o = _guarded(torch, (B, H_q, N_q, d), torch.bfloat16, -12345.0)
+    odt = torch.float16 if a.dtype == "f16" else torch.bfloat16
+    ob, o = _guarded(torch, (B, H_q, N_q, d), odt, -12345.0)
     lb, lse = _guarded(torch, (B, H_q, N_q), torch.float32, -12345.0)
     fn = fa.fa_naive_forward if naive else fa.fa_forward
     o2, lse2 = fn(q, k, v, causal=a.causal, scale=a.scale, out=o, lse=lse)
@@ -147,6 +148,42 @@ def test_causal_head_groups(fa, shape, group, monkeypatch):
     a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=9, k_row_frac=0.01)
     o, lse = _run(fa, a)
     compare(o, lse, *run_oracle(a))
+
+
+FP16 = [
+    (1, 1, 1, 17, 17, 128, True),
+    (1, 2, 1, 255, 255, 64, True),
+    (2, 8, 2, 300, 700, 128, True),      # GQA, N_q < N_k
+    (1, 4, 4, 600, 200, 64, True),       # N_q > N_k: leading rows see no key
+    (1, 1, 1, 2048, 8192, 128, False),   # split key ranges, in-cluster merge
+    (2, 8, 2, 2560, 2560, 64, True),     # more than a wave, causal head groups
+    (2, 8, 2, 4, 777, 128, True),        # decode path, ragged chunk
+    (16, 32, 8, 1, 8192, 128, False),    # decode workload's shape
+]
+
+
+@pytest.mark.parametrize("shape", FP16, ids=lambda s: "x".join(map(str, s[:6])) + ("c" if s[6] else ""))
+def test_fp16_parity(fa, shape):
+    # FP16 tensors through fa_forward_fp16: same kernels with FP16 operands, P and O
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=21, k_row_frac=0.01, dtype="f16")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a), elem="f16")
+
+
+@pytest.mark.parametrize("cluster_merge", [True, False], ids=["cluster", "kernel"])
+def test_fp16_split_merge_modes(fa, cluster_merge, monkeypatch):
+    monkeypatch.setenv("FA_CLUSTER_MERGE", "1" if cluster_merge else "0")
+    a = I.make_inputs(1, 2, 1, 1000, 6000, 128, causal=True, seed=22, dtype="f16")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a), elem="f16")
+
+
+def test_fp16_large_scores(fa):
+    # scores spread over many octaves: the lazy rescale keeps every FP16 P <= 2^15
+    a = I.make_inputs(1, 2, 2, 512, 4096, 128, causal=False, seed=23, scale=0.6, dtype="f16")
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a), elem="f16")
 
 
 def test_tiny_workload_n256_d64(fa):

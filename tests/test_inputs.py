@@ -51,3 +51,36 @@ def test_k_row_stress():
         assert np.array_equal(kf[bh, mask], bf[bh, mask] * 8)   # exact in bf16
         assert np.array_equal(kf[bh, ~mask], bf[bh, ~mask])
     assert np.array_equal(a.q, base.q) and np.array_equal(a.v, base.v)
+
+
+def test_f16_rounding_is_ieee_nearest_even():
+    # binary16: 10 fraction bits; ties go to the even neighbour, past the largest
+    # finite value (65504) the halfway point 65520 rounds to infinity, and the
+    # subnormal grid is 2^-24
+    x = np.array([1 + 2.0**-11, 1 + 3 * 2.0**-11, 1 + 2.0**-11 + 2.0**-30, 65504.0, 65519.99,
+                  65520.0, 2.0**-25, 3 * 2.0**-26, -2.0**-25, 2.0**-14 - 2.0**-25])
+    want = np.array([1.0, 1 + 2.0**-9, 1 + 2.0**-10, 65504.0, 65504.0, np.inf, 0.0, 2.0**-24,
+                     -0.0, 2.0**-14])
+    with np.errstate(over="ignore"):      # 65520 overflows on purpose
+        got = I.f64_to_f16(x).astype(np.float64)
+    assert np.array_equal(got, want)
+    assert np.signbit(got[8])
+
+
+def test_f16_inputs_follow_the_same_stream():
+    # the FP16 draw is the same deviates as the BF16 one, rounded to binary16
+    z = I.normal_f64(4, I.STREAM_V, 4096)
+    assert np.array_equal(I.normal_f16(4, I.STREAM_V, (4096,)), z.astype(np.float16))
+    a = I.make_inputs(1, 2, 1, 40, 300, 64, seed=4, k_row_frac=0.02, dtype="f16")
+    b = I.make_inputs(1, 2, 1, 40, 300, 64, seed=4, k_row_frac=0.02, dtype="bf16")
+    assert a.dtype == "f16" and a.q.dtype == np.float16 and b.q.dtype == np.uint16
+    # the scaled K rows are the same rows, and x8 is exact in binary16
+    plain = I.make_inputs(1, 2, 1, 40, 300, 64, seed=4, dtype="f16")
+    rows = I.scaled_rows(4, 1, 300, 0.02)[0]
+    assert np.array_equal(a.k[0, 0, rows].astype(np.float64), plain.k[0, 0, rows].astype(np.float64) * 8)
+    others = np.setdiff1d(np.arange(300), rows)
+    assert np.array_equal(a.k[0, 0, others], plain.k[0, 0, others])
+    # both roundings of one deviate are within their half-ulps of each other
+    qf = a.q.astype(np.float64)
+    qb = I.bf16_bits_to_f32(b.q).astype(np.float64)
+    assert np.all(np.abs(qf - qb) <= np.abs(qf) * (2.0**-8 + 2.0**-11) + 2.0**-24)
