@@ -299,89 +299,66 @@ def time_decode(fa, torch, dev, flush, stream, steps, warmup, world, dtype="bf16
 
 
 def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_per_step):
-    """End-to-end rate through the public API with host buffers (see the call site).
+    """End-to-end rate with the step's tensors in pinned host memory.
 
-    Returns (pipelined rate, pipelined ms per step, H2D bytes per step, D2H bytes
-    per step, {"value", "ms_per_step"} of the same steps run one after another on
-    one stream with nothing overlapped)."""
+    Fused: one ``fa_forward_host_packed`` call runs the K steps as K requests
+    (each copies Q | K | V in from one pinned buffer and O | LSE out to one of two
+    pinned buffers; libfa overlaps request i+1's copy in and i-1's copy out with
+    request i's kernels). ``serial``: the same steps as K calls of one request
+    each, nothing overlapped. Unfused: the serial form with torch copies.
+
+    Returns (rate, ms per step, H2D bytes per step, D2H bytes per step, serial dict)."""
     B, Hq, Hkv, Nq, Nk, d = a.shape_args
     nq, nk = a.q.size, a.k.size
+    el = elem_dtype(torch, a)
     hin = to_device(torch, np.concatenate([a.q.reshape(-1), a.k.reshape(-1), a.v.reshape(-1)]),
                     "cpu").pin_memory()
     o_bytes, l_bytes = B * Hq * Nq * d * 2, B * Hq * Nq * 4
-    din = [torch.empty_like(hin, device=dev) for _ in range(2)]
-    dout = [torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
     hout = [torch.empty(o_bytes + l_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    slots = []
-    for x, y in zip(din, dout):
-        slots.append((x[:nq].view(B, Hq, Nq, d), x[nq:nq + nk].view(B, Hkv, Nk, d),
-                      x[nq + nk:].view(B, Hkv, Nk, d),
-                      y[:o_bytes].view(elem_dtype(torch, a)).view(B, Hq, Nq, d),
-                      y[o_bytes:].view(torch.float32).view(B, Hq, Nq)))
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def forward(b):
-        qq, kk, vv, oo, ll = slots[b]
-        if ws is None:
-            fn(qq, kk, vv, causal=a.causal, scale=a.scale, out=oo, lse=ll)
-        else:
-            fn(qq, kk, vv, causal=a.causal, scale=a.scale, out=oo, lse=ll, workspace=ws)
+    if ws is None:
+        def run(n):
+            fa.fa_forward_host_packed([hin] * n, [hout[i & 1] for i in range(n)], a.shape_args,
+                                      causal=a.causal, scale=a.scale, dtype=el)
+    else:
+        din = torch.empty_like(hin, device=dev)
+        dq, dk, dv = (din[:nq].view(B, Hq, Nq, d), din[nq:nq + nk].view(B, Hkv, Nk, d),
+                      din[nq + nk:].view(B, Hkv, Nk, d))
+        dout = torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev)
+        do = dout[:o_bytes].view(el).view(B, Hq, Nq, d)
+        dl = dout[o_bytes:].view(torch.float32).view(B, Hq, Nq)
 
-    def pipelined(n):
-        ev_in = [torch.cuda.Event() for _ in range(n)]
-        ev_k = [torch.cuda.Event() for _ in range(n)]
-        ev_out = [torch.cuda.Event() for _ in range(n)]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_event(e0)
-        for i in range(n):
-            b = i & 1
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_k[i - 2])      # slot b's inputs read by step i-2
-                din[b].copy_(hin, non_blocking=True)
-                ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
-            if i >= 2:
-                stream.wait_event(ev_out[i - 2])      # slot b's outputs copied out by step i-2
-            forward(b)
-            ev_k[i].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_k[i])
-                hout[b].copy_(dout[b], non_blocking=True)
-                ev_out[i].record(s_out)
-        stream.wait_event(ev_out[n - 1])
-        e1.record(stream)
-        return e0, e1
+        def run(n):
+            for _ in range(n):
+                din.copy_(hin, non_blocking=True)
+                fn(dq, dk, dv, causal=a.causal, scale=a.scale, out=do, lse=dl, workspace=ws)
+                hout[0].copy_(dout, non_blocking=True)
 
-    def serial(n):
-        evs = []
-        for _ in range(n):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            din[0].copy_(hin, non_blocking=True)
-            forward(0)
-            hout[0].copy_(dout[0], non_blocking=True)
-            e1.record(stream)
-            evs.append((e0, e1))
-        return evs
-
-    pipelined(max(3, warmup))
+    run(max(3, warmup))
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    e0, e1 = pipelined(steps)
-    torch.cuda.synchronize()
-    p_ms = R.slowest_rank_ms(e0.elapsed_time(e1), world, dev)
-    serial(max(3, warmup))
-    torch.cuda.synchronize()
-    evs = serial(steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws is None:
+        e0.record(stream)
+        run(steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        p_ms = R.slowest_rank_ms(e0.elapsed_time(e1), world, dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for x0, x1 in evs:
+        x0.record(stream)
+        run(1)
+        x1.record(stream)
     torch.cuda.synchronize()
     s_ms = R.slowest_rank_ms(sum(x.elapsed_time(y) for x, y in evs), world, dev)
+    if ws is not None:
+        p_ms = s_ms
     return (R.whole_job_rate(work_per_step, steps, p_ms, world), p_ms / steps, hin.numel() * 2,
             hout[0].numel(),
             {"value": R.whole_job_rate(work_per_step, steps, s_ms, world), "ms_per_step": s_ms / steps,
-             "note": "the same steps one after another on one stream, nothing overlapped"})
+             "note": "the same steps as one request per call, nothing overlapped"})
 
 
 def main():
@@ -534,13 +511,9 @@ def main():
     flushed_ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in fev), world, dev)
     flushed_value = R.whole_job_rate(work_per_step, args.steps, flushed_ms, world)
 
-    # ---- end to end through the public API with host buffers. Each step copies
-    # its inputs in from one pinned host buffer (Q | K | V), runs the forward and
-    # copies O | LSE back to pinned host memory. Pipelined the way a caller would
-    # run a stream of requests: copies in and out go on their own streams into
-    # two device slots used in turn, so step i+1's copy in and step i-1's copy
-    # out overlap step i's kernels; the timed region runs from before the first
-    # copy in to after the last copy out.
+    # ---- end to end through the C ABI with host buffers: every step copies its
+    # inputs in from pinned host memory and its O | LSE back out, inside the
+    # timed region (fa_forward_host_packed; see time_e2e)
     e2e_value, e2e_ms_step, h2d, d2h, e2e_serial = time_e2e(
         torch, fa, a, cfg, dev, stream, fn, ws, args.steps, warmup, world, work_per_step)
 
@@ -596,8 +569,10 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step,
-                "note": ("pinned host buffers; copies in and out on their own streams into two "
-                         "device slots used in turn, overlapping the kernels of the step between"),
+                "note": ("fa_forward_host_packed: K requests in pinned host memory; libfa copies each in "
+                         "and out on its own streams through two device slots, overlapping the "
+                         "neighbouring requests' kernels" if args.impl == "fused" else
+                         "unfused path: torch copies around each call, nothing overlapped"),
                 "serial": e2e_serial},
         "gpu_launches": kernels_per_step * args.steps,
         "flushed": {"value": flushed_value, "unit": unit, "ms_per_step": flushed_ms / args.steps,

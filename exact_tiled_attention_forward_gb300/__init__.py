@@ -32,6 +32,9 @@ FA_ERR_NO_MEMORY = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
 
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP16 = 1
+
 _lib = None
 
 
@@ -49,6 +52,10 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 _SIGNATURES = {
     "fa_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_forward_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_forward_host": (_c_int, [_c_int] + [ctypes.POINTER(_vp)] * 5 + [_c_int] * 7 +
+                        [_c_float, _c_int, _vp]),
+    "fa_forward_host_packed": (_c_int, [_c_int] + [ctypes.POINTER(_vp)] * 2 + [_c_int] * 7 +
+                               [_c_float, _c_int, _vp]),
     "fa_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
@@ -157,6 +164,79 @@ def fa_forward_fp16(q, k, v, causal: bool = False, scale: float | None = None, o
                                N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "fa_forward_fp16")
     return out, lse
+
+
+def fa_forward_host(qs, ks, vs, outs, lses=None, causal: bool = False, scale: float | None = None,
+                    stream=None) -> None:
+    """n requests whose tensors are in host memory (lists of CPU tensors of one
+    shape and type, BF16 or FP16; page-locked memory lets the copies overlap the
+    kernels). Results land in ``outs`` (and ``lses`` when given) once ``stream``
+    has been synchronised; see ``include/fa.h``."""
+    import torch
+    n = len(qs)
+    if not (len(ks) == len(vs) == len(outs) == n) or (lses is not None and len(lses) != n):
+        raise ValueError("qs, ks, vs, outs (and lses) must have one entry per request")
+    if n == 0:
+        return
+    dtype = qs[0].dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q is {dtype}, expected torch.bfloat16 or torch.float16")
+    B, H_q, H_kv, N_q, N_k, d = _dims(qs[0], ks[0])
+    for i in range(n):
+        _check_dtypes(dtype, qs[i], ks[i], vs[i], outs[i], None if lses is None else lses[i])
+        group = [qs[i], ks[i], vs[i], outs[i]] + ([] if lses is None or lses[i] is None else [lses[i]])
+        for t in group:
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError("fa_forward_host takes contiguous CPU tensors")
+        if (qs[i].shape != qs[0].shape or ks[i].shape != ks[0].shape or vs[i].shape != ks[0].shape
+                or tuple(outs[i].shape) != (B, H_q, N_q, d)
+                or (lses is not None and lses[i] is not None and tuple(lses[i].shape) != (B, H_q, N_q))):
+            raise ValueError(f"request {i} does not have the shape of request 0")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+
+    def arr(ts):
+        return (_vp * n)(*[t.data_ptr() if t is not None else 0 for t in ts])
+
+    st = lib().fa_forward_host(n, arr(qs), arr(ks), arr(vs), arr(outs),
+                               None if lses is None else arr(lses), B, H_q, H_kv, N_q, N_k, d,
+                               int(bool(causal)), float(scale),
+                               FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16,
+                               _stream_ptr(stream))
+    _check(st, "fa_forward_host")
+
+
+def fa_forward_host_packed(qkvs, outs, shape, causal: bool = False, scale: float | None = None,
+                           dtype=None, stream=None) -> None:
+    """``fa_forward_host`` with each request packed in two contiguous CPU
+    buffers: ``qkvs[i]`` holds Q, K, V back to back and ``outs[i]`` receives O
+    then LSE (FP32). ``shape`` = (B, H_q, H_kv, N_q, N_k, d); ``dtype``
+    torch.bfloat16 (default) or torch.float16 names the element type."""
+    import torch
+    dtype = torch.bfloat16 if dtype is None else dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"dtype is {dtype}, expected torch.bfloat16 or torch.float16")
+    B, H_q, H_kv, N_q, N_k, d = (int(x) for x in shape)
+    n = len(qkvs)
+    if len(outs) != n:
+        raise ValueError("qkvs and outs must have one entry per request")
+    if n == 0:
+        return
+    in_bytes = (B * H_q * N_q + 2 * B * H_kv * N_k) * d * 2
+    out_bytes = B * H_q * N_q * (d * 2 + 4)
+    for t, need in [(t, in_bytes) for t in qkvs] + [(t, out_bytes) for t in outs]:
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("fa_forward_host_packed takes contiguous CPU buffers")
+        if t.numel() * t.element_size() < need:
+            raise ValueError(f"a buffer holds {t.numel() * t.element_size()} bytes, needs {need}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ptrs = lambda ts: (_vp * n)(*[t.data_ptr() for t in ts])
+    st = lib().fa_forward_host_packed(n, ptrs(qkvs), ptrs(outs), B, H_q, H_kv, N_q, N_k, d,
+                                      int(bool(causal)), float(scale),
+                                      FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16,
+                                      _stream_ptr(stream))
+    _check(st, "fa_forward_host_packed")
 
 
 def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None, out=None,

@@ -21,6 +21,7 @@ __device__ int g_device_status;  // one per device (module-scope device variable
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
+  cudaGetLastError();
   return FA_ERR_CUDA;
 }
 
@@ -103,8 +104,8 @@ __global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, long long rows, 
 }  // namespace
 
 int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st) {
-  fill_empty_kernel<<<256, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(o), lse, rows, d);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(fill_empty_kernel, dim3(256), dim3(256), 0, st,
+                                reinterpret_cast<__nv_bfloat16*>(o), lse, rows, d);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -513,8 +513,8 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
     kc.numAttrs = 1;
     e = cudaLaunchKernelEx(&kc, fa_decode_kernel<D, E>, tk, tv, p);
   } else {
-    fa_decode_kernel<D, E><<<(unsigned)ctas, kDecThreads, C::kSmemBytes, stream>>>(tk, tv, p);
-    e = cudaGetLastError();
+    e = launch_kernel(fa_decode_kernel<D, E>, dim3((unsigned)ctas), dim3(kDecThreads), C::kSmemBytes,
+                      stream, tk, tv, p);
   }
   if (e != cudaSuccess || p.cm) return e;
   const long long rows = (long long)p.B * p.H_kv * p.R;

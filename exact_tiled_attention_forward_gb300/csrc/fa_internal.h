@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace fa {
 
@@ -121,13 +122,29 @@ cudaError_t launch_row_softmax(const SoftmaxParams& p, cudaStream_t stream);
 struct Shape {
   int B, H_q, H_kv, N_q, N_k, d;
 };
+// Shape checks alone (sizes, H_q % H_kv, 32-bit row counts, d): fa_status code.
+int validate_shape(const Shape& s);
 // Argument checks shared by the forward entry points (fa_status code; FA_OK when valid).
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const Shape& s, float scale);
 // O = 0 and LSE = -inf for `rows` rows (every row sees no key).
 int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st);
-// Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA.
+// Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA; the
+// runtime's per-thread last error is cleared (the code now carries it).
 int cuda_fail(cudaError_t e);
+
+// Launch whose return value is that launch's own status (cudaLaunchKernelEx),
+// not the thread's last error, which an earlier unrelated call may have left set.
+template <typename... K, typename... A>
+inline cudaError_t launch_kernel(void (*kernel)(K...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, A&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 int num_sms();
 extern thread_local int g_last_cuda_error;
 

@@ -242,8 +242,8 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
     attr = true;
   }
   dim3 grid((p.N + BN - 1) / BN, (p.M + 127) / 128, p.batches);
-  gemm_bf16_kernel<BN, B_MN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(ta, tb, p, status);
-  return cudaGetLastError();
+  return launch_kernel(gemm_bf16_kernel<BN, B_MN>, grid, dim3(kGemmThreads), C::kSmemBytes, stream, ta, tb,
+                       p, status);
 }
 
 }  // namespace
@@ -265,8 +265,7 @@ cudaError_t launch_gemm(bool b_mn_major, int bn, const CUtensorMap& ta, const CU
 
 cudaError_t launch_row_softmax(const SoftmaxParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  row_softmax_kernel<<<p.rows, kSmThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(row_softmax_kernel, dim3((unsigned)p.rows), dim3(kSmThreads), 0, stream, p);
 }
 
 }  // namespace fa

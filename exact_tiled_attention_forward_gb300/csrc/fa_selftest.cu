@@ -29,7 +29,7 @@ extern "C" int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* str
   if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
   int* status = fa::device_status_ptr();
   if (!status) return fa::cuda_fail(cudaGetLastError());
-  fa::fa_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, timeout_ns);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = fa::launch_kernel(fa::fa_selftest_wait_kernel, dim3(1), dim3(32), 0,
+                                          static_cast<cudaStream_t>(stream), status, timeout_ns);
   return e == cudaSuccess ? FA_OK : fa::cuda_fail(e);
 }

@@ -56,6 +56,9 @@ typedef enum {
   FA_ERR_TOO_LARGE = -6    /* fa_forward_noalloc: needs more than its static scratch holds */
 } fa_status;
 
+/* Element type of q, k, v and o for the entry points that take one. */
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 } fa_dtype;
+
 /* Exact attention forward, fused (the tiled online-softmax kernel).
  * Prefill: tcgen05/TMA kernel, two 128-row query tiles per CTA, K/V tiles of
  * 128 keys. Query blocks that do not fill a whole wave of the GPU have their
@@ -91,6 +94,42 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
                     void* stream);
+
+/* n forward requests of one shape whose tensors live in HOST memory (no
+ * counterpart on the pages, which start from tensors in device memory: this is
+ * the serving-side runtime around the same path). For request i, q[i], k[i],
+ * v[i] are host pointers to its inputs and o[i], lse[i] to its outputs, in
+ * fa_forward's layouts; `lse` (the array) or any lse[i] may be NULL (that LSE is
+ * not copied back). dtype: FA_DTYPE_BF16 (fa_forward) or FA_DTYPE_FP16
+ * (fa_forward_fp16). Host pointers need no alignment; page-locked memory
+ * (cudaHostAlloc, cudaHostRegister) lets the copies run asynchronously.
+ * Execution: each request's inputs are copied into one of two device slots
+ * (stream-ordered memory from libfa's pool, on `stream`), the fused forward
+ * runs on `stream`, and O, LSE are copied back. The copies run on two
+ * library-owned streams of the current device, so request i+1's copy in and
+ * request i-1's copy out overlap request i's kernels. Each tensor is its own
+ * copy (fa_forward_host_packed moves a request with one copy each way).
+ * Ordering: all of it runs after the work already on `stream`, and work
+ * enqueued on `stream` later runs after all of it; the call returns once
+ * everything is enqueued, so synchronise `stream` before reading outputs or
+ * reusing inputs. Concurrent calls on one device enqueue one at a time.
+ * Returns FA_OK; FA_ERR_INVALID_ARG (n < 0, NULL arrays or request pointers,
+ * bad shape or scale, unknown dtype) or FA_ERR_UNSUPPORTED before anything is
+ * enqueued; FA_ERR_NO_MEMORY if the slots cannot be allocated; FA_ERR_CUDA if a
+ * copy or launch fails (requests before the failing one may have run; the
+ * caller's stream still waits for everything that was enqueued). */
+int fa_forward_host(int n, const void* const* q, const void* const* k, const void* const* v,
+                    void* const* o, float* const* lse, int B, int H_q, int H_kv, int N_q, int N_k,
+                    int d, int causal, float scale, int dtype, void* stream);
+
+/* fa_forward_host with each request packed into two host buffers: qkv[i]
+ * holds Q, K and V back to back (Q first, then K, then V, each in fa_forward's
+ * layout, no padding) and out[i] receives O followed by LSE (FP32). Each
+ * request then moves with one copy in and one copy out, which runs closer to
+ * the host link's rate than several smaller copies. Everything else as
+ * fa_forward_host. */
+int fa_forward_host_packed(int n, const void* const* qkv, void* const* out, int B, int H_q, int H_kv,
+                           int N_q, int N_k, int d, int causal, float scale, int dtype, void* stream);
 
 /* fa_forward without any device-memory allocation. (The pages have no
  * counterpart: this exists for callers, not for the method.)

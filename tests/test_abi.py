@@ -25,7 +25,9 @@ def lib():
 
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
-    assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_noalloc", "fa_naive_forward",
+    assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_host", "fa_forward_host_packed",
+                          "fa_forward_noalloc",
+                          "fa_naive_forward",
                           "fa_naive_workspace_bytes", "fa_forward_plan", "fa_selftest_wait_timeout",
                           "fa_status_string", "fa_get_last_cuda_error", "fa_device_status",
                           "fa_version"}
@@ -150,3 +152,55 @@ def test_binding_checks_element_types():
         fa.fa_naive_forward(q16, q16, q16)
     with pytest.raises(TypeError):
         fa.fa_forward(qb, qb, qb, lse=torch.zeros(1, 1, 8, dtype=torch.float16))
+
+
+def test_host_batch_rejects(lib):
+    f = lib.fa_forward_host
+    P = ctypes.c_void_p
+    one = (P * 1)(0x1000)
+    two = (P * 2)(0x1000, 0)                 # request 1 has a NULL pointer
+    args = (1, 2, 1, 64, 64, 128, 0, 0.1, 0, None)
+    assert f(0, None, None, None, None, None, *args) == fa.FA_OK          # nothing to do
+    assert f(-1, one, one, one, one, None, *args) == fa.FA_ERR_INVALID_ARG
+    assert f(1, None, one, one, one, None, *args) == fa.FA_ERR_INVALID_ARG
+    assert f(2, two, two, two, two, None, *args) == fa.FA_ERR_INVALID_ARG
+    assert f(1, one, one, one, one, None, 1, 3, 2, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, one, one, one, one, None, 1, 2, 1, 64, 64, 96, 0, 0.1, 0, None) == fa.FA_ERR_UNSUPPORTED
+    assert f(1, one, one, one, one, None, 1, 2, 1, 64, 64, 128, 0, float("nan"), 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, one, one, one, one, None, 1, 2, 1, 64, 64, 128, 0, 0.1, 7, None) == fa.FA_ERR_INVALID_ARG
+    # an empty query set is a no-op whatever the pointers
+    assert f(1, (P * 1)(0), (P * 1)(0), (P * 1)(0), (P * 1)(0), None, 1, 2, 1, 0, 64, 128, 0, 0.1, 0,
+             None) == fa.FA_OK
+
+
+def test_host_batch_binding_checks():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_forward_host([q], [k], [k, k], [o])                     # lists of unequal length
+    with pytest.raises(ValueError):
+        fa.fa_forward_host([q, q[:, :1].contiguous()], [k, k], [k, k], [o, o])   # shapes differ
+    with pytest.raises(TypeError):
+        fa.fa_forward_host([q], [k], [k], [o.half()])
+    with pytest.raises(ValueError):
+        fa.fa_forward_host([q.transpose(2, 3)], [k], [k], [o])       # not contiguous
+    fa.fa_forward_host([], [], [], [])                                # nothing to do
+
+
+def test_host_packed_rejects(lib):
+    f = lib.fa_forward_host_packed
+    P = ctypes.c_void_p
+    one = (P * 1)(0x1000)
+    assert f(0, None, None, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_OK
+    assert f(-1, one, one, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, None, one, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, one, None, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, (P * 1)(0), one, 1, 2, 1, 64, 64, 128, 0, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert f(1, one, one, 1, 2, 1, 64, 64, 80, 0, 0.1, 0, None) == fa.FA_ERR_UNSUPPORTED
+    assert f(1, one, one, 1, 2, 1, 64, 64, 128, 0, 0.1, 2, None) == fa.FA_ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):       # a buffer too small for the shape
+        fa.fa_forward_host_packed([torch.zeros(10, dtype=torch.uint8)], [torch.zeros(10, dtype=torch.uint8)],
+                                  (1, 1, 1, 8, 8, 64))
