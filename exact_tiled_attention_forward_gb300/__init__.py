@@ -98,10 +98,15 @@ def _check(status: int, what: str):
 
 
 def _stream_ptr(stream):
-    import torch
+    """Raw handle of `stream` (a torch stream or an int), or of the current
+    stream of the current device when None."""
     if stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)   # ~10x cheaper than current_stream()
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _dims(q, k):
@@ -113,7 +118,9 @@ def _dims(q, k):
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
+    """Device address of a tensor as an int (0 for None or an empty tensor); the
+    c_void_p argtypes take ints directly."""
+    return t.data_ptr() if t is not None and t.numel() > 0 else 0
 
 
 def _check_dtypes(dtype, q, k, v, out, lse):
