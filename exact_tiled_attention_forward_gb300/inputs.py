@@ -33,7 +33,7 @@ GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_ROWS = 1, 2, 3, 4
+STREAM_Q, STREAM_K, STREAM_V, STREAM_ROWS, STREAM_DO = 1, 2, 3, 4, 5
 
 _CHUNK = 1 << 22  # elements generated per numpy pass (bounds temporaries)
 
@@ -178,6 +178,12 @@ def make_inputs(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int, *,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     return AttentionInputs(q, k, v, B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale), dtype)
+
+
+def grad_output(a: AttentionInputs, seed: int = 0) -> np.ndarray:
+    """dO for a backward pass of `a`: N(0, 1) in a's storage type, shaped like O."""
+    shape = (a.B, a.H_q, a.N_q, a.d)
+    return normal_f16(seed, STREAM_DO, shape) if a.dtype == "f16" else normal_bf16(seed, STREAM_DO, shape)
 
 
 # The five workloads the method is measured on (batch, heads, lengths, head dim,

@@ -15,6 +15,8 @@ Contents
                tiled online-softmax restatement used as a self-check; a
                pure-Python brute force for tiny shapes; the split merge.
 ``traffic``    the pages' analytic HBM byte and FLOP counts.
+``backward``   FP64 gradients dQ, dK, dV of the definition (chain rule, pinned by
+               finite differences of the forward).
 
 Every function names the page and section it follows. Each is pinned in
 ``tests/test_oracle_*.py`` against values the pages print, closed forms and
@@ -32,3 +34,4 @@ from .attention import (  # noqa: F401
     visible_key_count,
 )
 from . import traffic  # noqa: F401
+from .backward import attention_backward, forward_loss  # noqa: F401

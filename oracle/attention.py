@@ -42,10 +42,10 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def to_f64(x: np.ndarray) -> np.ndarray:
-    """Exact widening of an input tensor to float64: IEEE binary16 values
-    (numpy.float16 arrays) directly, anything else as bfloat16 bit patterns."""
+    """Exact widening of an input tensor to float64: floating-point arrays
+    (binary16, 32, 64) by value, 16-bit integer arrays as bfloat16 bit patterns."""
     x = np.asarray(x)
-    if x.dtype == np.float16:
+    if np.issubdtype(x.dtype, np.floating):
         return x.astype(np.float64)
     return bf16_to_f64(x)
 

@@ -1,0 +1,89 @@
+"""Pins of the FP64 backward oracle against things other than itself: central
+finite differences of the forward oracle (the gradient of sum(dO * O)), closed
+forms and invariants of the softmax Jacobian."""
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_forward_gb300 import inputs as I
+
+SHAPES = [
+    # (B, H_q, H_kv, N_q, N_k, d, causal)
+    (1, 2, 1, 5, 7, 4, True),      # GQA, N_q < N_k
+    (1, 2, 2, 6, 4, 3, False),
+    (2, 4, 2, 3, 5, 4, True),
+    (1, 1, 1, 6, 3, 4, True),      # N_q > N_k: the first rows see no key
+]
+
+
+def _random(shape, seed):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    rng = np.random.default_rng(seed)
+    return (rng.normal(size=(B, Hq, Nq, d)), rng.normal(size=(B, Hkv, Nk, d)),
+            rng.normal(size=(B, Hkv, Nk, d)), rng.normal(size=(B, Hq, Nq, d)), causal)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_gradients_match_central_differences(shape):
+    q, k, v, do, causal = _random(shape, 11)
+    scale = 0.7
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=causal, scale=scale)
+    h = 1e-5
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            keep = x[idx]
+            x[idx] = keep + h
+            up = oracle.forward_loss(q, k, v, do, causal=causal, scale=scale)
+            x[idx] = keep - h
+            dn = oracle.forward_loss(q, k, v, do, causal=causal, scale=scale)
+            x[idx] = keep
+            fd[idx] = (up - dn) / (2 * h)
+        np.testing.assert_allclose(g, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_equal_value_rows_give_no_query_or_key_gradient():
+    # O = c for every row whatever P is, so S (hence Q, K) cannot move the loss
+    q, k, v, do, _ = _random((1, 2, 1, 6, 9, 4, False), 12)
+    v[:] = v[:, :, :1]
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=False, scale=0.5)
+    assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+    assert np.abs(dv).max() > 0.1
+
+
+def test_zero_upstream_gradient():
+    q, k, v, do, _ = _random((1, 1, 1, 4, 4, 4, True), 13)
+    grads = oracle.attention_backward(q, k, v, np.zeros_like(do), causal=True)
+    assert all(np.abs(x).max() == 0.0 for x in grads)
+
+
+def test_query_gradient_ignores_a_shift_of_all_keys():
+    # rows of dS sum to zero (softmax Jacobian), so dQ = scale dS K is blind to K + u
+    q, k, v, do, _ = _random((1, 2, 2, 5, 8, 4, False), 14)
+    dq, dk, _ = oracle.attention_backward(q, k, v, do, causal=False, scale=0.3)
+    u = np.array([0.5, -1.0, 2.0, 0.25])
+    q2, k2 = q.copy(), k + u
+    # shifting K also shifts the scores by q . u per row: a per-row constant, so P is unchanged
+    dq2, dk2, _ = oracle.attention_backward(q2, k2, v, do, causal=False, scale=0.3)
+    np.testing.assert_allclose(dq2, dq, atol=1e-12)
+
+
+def test_gqa_equals_repeated_heads_summed():
+    q, k, v, do, _ = _random((1, 4, 2, 5, 6, 4, True), 15)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True, scale=0.6)
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    dq_m, dk_m, dv_m = oracle.attention_backward(q, kr, vr, do, causal=True, scale=0.6)
+    np.testing.assert_allclose(dq, dq_m, atol=1e-13)
+    np.testing.assert_allclose(dk, dk_m.reshape(1, 2, 2, 6, 4).sum(axis=2), atol=1e-13)
+    np.testing.assert_allclose(dv, dv_m.reshape(1, 2, 2, 6, 4).sum(axis=2), atol=1e-13)
+
+
+def test_bits_inputs_widen_exactly():
+    # BF16 bit patterns and their float64 values give the same gradients
+    a = I.make_inputs(1, 2, 1, 7, 9, 8, causal=True, seed=3)
+    do = I.grad_output(a, seed=3)
+    g_bits = oracle.attention_backward(a.q, a.k, a.v, do, causal=True, scale=a.scale)
+    w = oracle.to_f64
+    g_f64 = oracle.attention_backward(w(a.q), w(a.k), w(a.v), w(do), causal=True, scale=a.scale)
+    for x, y in zip(g_bits, g_f64):
+        assert np.array_equal(x, y)
