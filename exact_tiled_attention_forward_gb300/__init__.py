@@ -57,6 +57,7 @@ _SIGNATURES = {
     "fa_forward_host_packed": (_c_int, [_c_int] + [ctypes.POINTER(_vp)] * 2 + [_c_int] * 7 +
                                [_c_float, _c_int, _vp]),
     "fa_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_backward": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _c_int, _vp]),
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
     "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
@@ -244,6 +245,33 @@ def fa_forward_host_packed(qkvs, outs, shape, causal: bool = False, scale: float
                                       FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16,
                                       _stream_ptr(stream))
     _check(st, "fa_forward_host_packed")
+
+
+def fa_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None,
+                dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of the forward given its o and lse and the upstream
+    gradient do; BF16 or FP16 tensors (all one type), FP32 lse. Returns (dq, dk, dv)."""
+    import torch
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q is {dtype}, expected torch.bfloat16 or torch.float16")
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is not None and t.dtype != dtype:
+            raise TypeError(f"{name} is {t.dtype}, expected {dtype}")
+    if lse is None or lse.dtype != torch.float32:
+        raise TypeError("lse (FP32, from the forward) is required")
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib().fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, H_q, H_kv, N_q, N_k, d, int(bool(causal)), float(scale),
+                           FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16,
+                           _stream_ptr(stream))
+    _check(st, "fa_backward")
+    return dq, dk, dv
 
 
 def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None, out=None,

@@ -131,6 +131,24 @@ int fa_forward_host(int n, const void* const* q, const void* const* k, const voi
 int fa_forward_host_packed(int n, const void* const* qkv, void* const* out, int B, int H_q, int H_kv,
                            int N_q, int N_k, int d, int causal, float scale, int dtype, void* stream);
 
+/* Gradients of the exact attention forward: given q, k, v, the forward's o and
+ * lse (FP32, required) and the upstream gradient dout (= dL/dO, o's layout),
+ * writes dq (q's layout), dk and dv (k's layout), all of element type dtype
+ * (FA_DTYPE_BF16 or FA_DTYPE_FP16) with FP32 accumulation. Same scale, causal
+ * and GQA conventions as fa_forward: dk and dv of a KV head sum over the query
+ * heads that read it. The scores are recomputed tile by tile from q, k and the
+ * saved lse, not stored ("Why is standard attention memory-bound...", Step 4).
+ * Work: a per-row preprocessing kernel (D = rowsum(dout * o)), a dK/dV kernel
+ * over key blocks and a dQ kernel over query tiles, on `stream`, with two
+ * B*H_q*roundup(N_q, 128) FP32 arrays of stream-ordered workspace from libfa's
+ * pool. Deterministic (no atomics). Pointers: device, 16-byte aligned; the
+ * outputs may not overlap any input or each other. When N_q or N_k is 0 the
+ * gradients that exist are zero-filled. Returns FA_OK, FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED (d not 64/128), FA_ERR_NO_MEMORY or FA_ERR_CUDA. */
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N_q,
+                int N_k, int d, int causal, float scale, int dtype, void* stream);
+
 /* fa_forward without any device-memory allocation. (The pages have no
  * counterpart: this exists for callers, not for the method.)
  * For callers that cannot allocate device memory on this path: a serving loop

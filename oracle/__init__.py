@@ -34,4 +34,4 @@ from .attention import (  # noqa: F401
     visible_key_count,
 )
 from . import traffic  # noqa: F401
-from .backward import attention_backward, forward_loss  # noqa: F401
+from .backward import attention_backward, backward_error_terms, forward_loss  # noqa: F401

@@ -77,3 +77,37 @@ def forward_loss(q, k, v, do, causal: bool = False, scale: float | None = None) 
     from .attention import attention_reference
     o, _ = attention_reference(q, k, v, causal=causal, scale=scale)
     return float((to_f64(do) * o).sum())
+
+
+def backward_error_terms(q, k, v, do, causal: bool = False, scale: float | None = None):
+    """Magnitudes that bound what rounding the method's own precision does to
+    each gradient (for the tolerance of a 16-bit backward; FP64, same shapes as
+    attention_backward's results):
+
+    * dQ: scale |dS| |K|  +  scale Dabs * (P |K|), with Dabs_i = sum_t |dO_it O_it|
+      (dS is rounded before the dS K product; O enters D rounded to 16 bits);
+    * dK: scale |dS|^T |Q|  +  scale P^T (Dabs * |Q|);
+    * dV: P^T |dO| (P is rounded before the P^T dO product).
+    A gradient computed with unit roundoff u is within about u (terms + |gradient|)."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    B, H_q, n_q, d = q.shape
+    H_kv, n_k = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    g = H_q // H_kv
+    tq = np.zeros_like(q)
+    tk = np.zeros_like(k)
+    tv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H_q):
+            hk = h // g
+            qh, kh, vh, doh = q[b, h], k[b, hk], v[b, hk], do[b, h]
+            p = _probabilities(qh, kh, n_q, n_k, causal, scale)
+            o = p @ vh
+            dp = doh @ vh.T
+            ds = p * (dp - (doh * o).sum(axis=1, keepdims=True))
+            dabs = np.abs(doh * o).sum(axis=1, keepdims=True)
+            tq[b, h] = scale * (np.abs(ds) @ np.abs(kh) + dabs * (p @ np.abs(kh)))
+            tk[b, hk] += scale * (np.abs(ds).T @ np.abs(qh) + p.T @ (dabs * np.abs(qh)))
+            tv[b, hk] += p.T @ np.abs(doh)
+    return tq, tk, tv

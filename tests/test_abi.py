@@ -26,6 +26,7 @@ def lib():
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
     assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_host", "fa_forward_host_packed",
+                          "fa_backward",
                           "fa_forward_noalloc",
                           "fa_naive_forward",
                           "fa_naive_workspace_bytes", "fa_forward_plan", "fa_selftest_wait_timeout",
@@ -204,3 +205,29 @@ def test_host_packed_rejects(lib):
     with pytest.raises(ValueError):       # a buffer too small for the shape
         fa.fa_forward_host_packed([torch.zeros(10, dtype=torch.uint8)], [torch.zeros(10, dtype=torch.uint8)],
                                   (1, 1, 1, 8, 8, 64))
+
+
+def test_backward_rejects(lib):
+    f = lib.fa_backward
+    # q, k, v, o, lse, do, dq, dk, dv
+    ok_ptrs = [0x10000000 * (i + 1) for i in range(9)]         # disjoint, 16-byte aligned
+    args = (1, 2, 1, 64, 64, 128, 0, 0.1, 0, None)
+    def call(**kw):
+        p = list(ok_ptrs)
+        for i, name in enumerate(["q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"]):
+            if name in kw:
+                p[i] = kw[name]
+        a = list(args)
+        for i, name in enumerate(["B", "Hq", "Hkv", "Nq", "Nk", "d", "causal", "scale", "dtype"]):
+            if name in kw:
+                a[i] = kw[name]
+        return f(*p, *a)
+    assert call(Hq=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=3) == fa.FA_ERR_INVALID_ARG
+    assert call(lse=0) == fa.FA_ERR_INVALID_ARG                   # lse is required
+    assert call(do=0x60000008) == fa.FA_ERR_INVALID_ARG            # misaligned
+    assert call(dq=0x10000000 + 64) == fa.FA_ERR_INVALID_ARG       # dq overlaps q
+    assert call(dk=0x70000000) == fa.FA_ERR_INVALID_ARG            # dk overlaps dq
+    assert call(dv=0x30000000) == fa.FA_ERR_INVALID_ARG            # dv aliases v
