@@ -68,9 +68,11 @@ struct BwdCfg {
   static constexpr int kOffStages = kOffResVec + 1024;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kOffBar = kOffStages + kStages * kStageBytes;
+  // kBarS + h / kBarP + h: half h of the score-shaped products done / its
+  // element-wise results stored (h = 0, 1)
   static constexpr int kBarRes = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
-                       kBarP = 2 + 2 * kStages, kBarDone = 3 + 2 * kStages, kBarDrain = 4 + 2 * kStages,
-                       kNumBars = 5 + 2 * kStages;
+                       kBarP = 3 + 2 * kStages, kBarDone = 5 + 2 * kStages, kBarDrain = 6 + 2 * kStages,
+                       kNumBars = 7 + 2 * kStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   // launched with at least 116 KiB so that one CTA holds an SM: each CTA takes all
@@ -78,8 +80,10 @@ struct BwdCfg {
   static constexpr int kLaunchSmem = kSmemBytes < 116 * 1024 ? 116 * 1024 : kSmemBytes;
   static_assert(kLaunchSmem <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
-  // tensor memory: [0,128) S or S^T (P / P^T over its first 64 columns),
-  // [128,256) dP or dP^T (dS / dS^T), [256,256+D) dV or dQ, [384,384+D) dK
+  // tensor memory: [0,128) S or S^T, [128,256) dP or dP^T, each as two halves
+  // of 64 columns (P / P^T packed over the first 32 columns of its S half,
+  // dS / dS^T over the first 32 of its dP half); [256,256+D) dV or dQ,
+  // [384,384+D) dK
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmA = 256, kTmB = 384;
 };
 
@@ -203,8 +207,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarS), 1);
-    mbar_init(bar(C::kBarP), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kBarS + h), 1);
+      mbar_init(bar(C::kBarP + h), 128);
+    }
     mbar_init(bar(C::kBarDone), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *s_abort = 0;
@@ -261,47 +267,73 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdWarpMma) {
     if (n_steps > 0) {
-      constexpr uint32_t idS = idesc_f32(128, kT, false, E);
+      constexpr uint32_t idS = idesc_f32(128, kT / 2, false, E);   // one half: 64 query rows
       constexpr uint32_t idO = idesc_f32(128, D, true, E);
       constexpr uint32_t kHi = desc_sw128_hi(1024);
       constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
+      constexpr uint32_t kHalfRows16 = (kT / 2) * 128 / 16;     // 64 rows of a 128-byte box, 16-byte units
       const uint32_t lk = desc_sw128_lo(sb + C::kOffRes, 16);
       const uint32_t lv = desc_sw128_lo(sb + C::kOffRes + C::kTileBytes, 16);
-      bool ok = mbar_wait_w(bar(C::kBarRes), 0, s_abort, p.status);
+      // S^T = K Q^T and dP^T = V dO^T for the query rows of half h of step i
+      // (keys on the lanes, 64 columns each), K-steps of 16 over d
+      auto scores = [&](int i, int h) {
+        const uint32_t sq = sb + C::kOffStages + (i % C::kStages) * C::kStageBytes;
+        const uint32_t lq = desc_sw128_lo(sq, 16) + (uint32_t)h * kHalfRows16;
+        const uint32_t ldo = desc_sw128_lo(sq + C::kTileBytes, 16) + (uint32_t)h * kHalfRows16;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+          mma_ss_lh_w(tmem + C::kTmS + 64u * h, lk + off, kHi, lq + off, kHi, idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+          mma_ss_lh_w(tmem + C::kTmP + 64u * h, lv + off, kHi, ldo + off, kHi, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(bar(C::kBarS + h));
+      };
+      bool ok = mbar_wait_w(bar(C::kBarRes), 0, s_abort, p.status) &&
+                mbar_wait_w(bar(C::kBarFull + 0), 0, s_abort, p.status);
+      if (ok) {
+        tc_fence_after();
+        scores(0, 0);
+        scores(0, 1);
+      }
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::kStages;
-        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-        if (!(ok = mbar_wait_w(bar(C::kBarFull + st), ph, s_abort, p.status))) break;
-        tc_fence_after();
         const uint32_t sq = sb + C::kOffStages + st * C::kStageBytes;
-        const uint32_t lq = desc_sw128_lo(sq, 16), ldo = desc_sw128_lo(sq + C::kTileBytes, 16);
-        // S^T = K Q^T and dP^T = V dO^T (keys on the lanes), K-steps of 16 over d
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-          mma_ss_lh_w(tmem + C::kTmS, lk + off, kHi, lq + off, kHi, idS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-          mma_ss_lh_w(tmem + C::kTmP, lv + off, kHi, ldo + off, kHi, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(bar(C::kBarS));
-        if (!(ok = mbar_wait_w(bar(C::kBarP), (uint32_t)i & 1u, s_abort, p.status))) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q: A (keys x rows) from tensor memory, B the
-        // row-major tile as an MN-major operand; K-steps of 16 rows
         const uint32_t bdo = desc_sw128_lo(sq + C::kTileBytes, C::kBoxBytes);
         const uint32_t bq = desc_sw128_lo(sq, C::kBoxBytes);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait_w(bar(C::kBarP + h), (uint32_t)i & 1u, s_abort, p.status))) break;
+          tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q over the 64 rows of half h: A (keys x
+          // rows) from tensor memory, B the row-major tile as an MN-major
+          // operand; K-steps of 16 rows
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + (uint32_t)kk * 8u, bdo + (uint32_t)kk * (16u * 128u >> 4),
-                      kHi, idO, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kT / 32; ++kk)
+            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + 64u * h + (uint32_t)kk * 8u,
+                        bdo + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
+                        (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts_lh_w(tmem + C::kTmB, tmem + C::kTmP + (uint32_t)kk * 8u, bq + (uint32_t)kk * (16u * 128u >> 4),
-                      kHi, idO, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(bar(C::kBarEmpty + st));
+          for (int kk = 0; kk < kT / 32; ++kk)
+            mma_ts_lh_w(tmem + C::kTmB, tmem + C::kTmP + 64u * h + (uint32_t)kk * 8u,
+                        bq + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
+                        (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          if (h == 1) mma_commit_w(bar(C::kBarEmpty + st));   // the stage's last reader
+          if (i + 1 < n_steps) {
+            // half h of the next step's scores, behind this half's products in
+            // the pipe (they read the columns the new scores overwrite)
+            if (h == 0) {
+              const int i1 = i + 1;
+              if (!(ok = mbar_wait_w(bar(C::kBarFull + i1 % C::kStages), (uint32_t)(i1 / C::kStages) & 1u,
+                                     s_abort, p.status)))
+                break;
+              tc_fence_after();
+            }
+            scores(i + 1, h);
+          }
+        }
       }
       mma_commit_w(bar(C::kBarDone));
       mma_commit_w(bar(C::kBarDrain));
@@ -316,41 +348,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tmem + lane_base + C::kTmS, tP = tmem + lane_base + C::kTmP;
     const float c = p.c;
     bool ok = true;
-    for (int i = 0; i < n_steps; ++i) {
-      if (!(ok = mbar_wait_w(bar(C::kBarS), (uint32_t)i & 1u, s_abort, p.status))) break;
-      tc_fence_after();
+    for (int i = 0; i < n_steps && ok; ++i) {
       const int st = i % C::kStages;
-      // the stage's lse2 / D vectors came by TMA: observe their barrier directly
-      // (it cannot move on before this thread publishes P^T for this step)
-      if (!(ok = mbar_wait_w(bar(C::kBarFull + st), (uint32_t)(i / C::kStages) & 1u, s_abort, p.status))) break;
       const int hl = i / n_t, t = t_lo + (i - hl * n_t);
       const int q0 = t * kT;
       const float* vl = reinterpret_cast<const float*>(smem + C::kOffStages + st * C::kStageBytes + 2 * C::kTileBytes);
       const float* vd = vl + kT;
       // rows r with key > row + kv_off are masked (causal)
       const int r_min = p.causal ? key - p.kv_off - q0 : -1;   // rows below r_min see no key k
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_w(bar(C::kBarS + h), (uint32_t)i & 1u, s_abort, p.status))) break;
+        tc_fence_after();
+        // the stage's lse2 / D vectors came by TMA: observe their barrier directly
+        // (it cannot move on before this thread publishes this step's second half)
+        if (h == 0 &&
+            !(ok = mbar_wait_w(bar(C::kBarFull + st), (uint32_t)(i / C::kStages) & 1u, s_abort, p.status)))
+          break;
+        const uint32_t hS = tS + 64u * h, hP = tP + 64u * h;
 #pragma unroll 1
-      for (int cc = 0; cc < kT; cc += 32) {
-        float s[32], dp[32];
-        tmem_ld32(tS + (uint32_t)cc, s);
-        tmem_ld32(tP + (uint32_t)cc, dp);
-        tmem_wait_ld();
-        uint32_t pk[16], dk2[16];
+        for (int cc = 0; cc < kT / 2; cc += 32) {
+          float s[32], dp[32];
+          tmem_ld32(hS + (uint32_t)cc, s);
+          tmem_ld32(hP + (uint32_t)cc, dp);
+          tmem_wait_ld();
+          uint32_t pk[16], dk2[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int r = cc + e;
-          float p0 = ex2_approx(s[e] * c - vl[r]);
-          float p1 = ex2_approx(s[e + 1] * c - vl[r + 1]);
-          if (r < r_min) p0 = 0.f;
-          if (r + 1 < r_min) p1 = 0.f;
-          pk[e >> 1] = pack2<E>(p0, p1);
-          dk2[e >> 1] = pack2<E>(p0 * (dp[e] - vd[r]), p1 * (dp[e + 1] - vd[r + 1]));
+          for (int e = 0; e < 32; e += 2) {
+            const int r = 64 * h + cc + e;
+            float p0 = ex2_approx(s[e] * c - vl[r]);
+            float p1 = ex2_approx(s[e + 1] * c - vl[r + 1]);
+            if (r < r_min) p0 = 0.f;
+            if (r + 1 < r_min) p1 = 0.f;
+            pk[e >> 1] = pack2<E>(p0, p1);
+            dk2[e >> 1] = pack2<E>(p0 * (dp[e] - vd[r]), p1 * (dp[e + 1] - vd[r + 1]));
+          }
+          // over columns already read: P^T / dS^T of the half's rows cc .. cc+31
+          // in its columns cc/2 ..
+          tmem_st16(hS + (uint32_t)(cc >> 1), pk);
+          tmem_st16(hP + (uint32_t)(cc >> 1), dk2);
         }
-        // over columns already read: P^T / dS^T of rows cc .. cc+31 in columns cc/2 ..
-        tmem_st16(tS + (uint32_t)(cc >> 1), pk);
-        tmem_st16(tP + (uint32_t)(cc >> 1), dk2);
+        bwd_publish(bar(C::kBarP + h));
       }
-      bwd_publish(bar(C::kBarP));
     }
     if (ok && n_steps > 0) {
       ok = mbar_wait_w(bar(C::kBarDone), 0, s_abort, p.status);
@@ -405,8 +443,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarS), 1);
-    mbar_init(bar(C::kBarP), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kBarS + h), 1);
+      mbar_init(bar(C::kBarP + h), 128);
+    }
     mbar_init(bar(C::kBarDone), 1);
     mbar_init(bar(C::kBarDrain), 1);
     *s_abort = 0;
@@ -459,41 +499,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdWarpMma) {
     if (n_steps > 0) {
-      constexpr uint32_t idS = idesc_f32(128, kT, false, E);
+      constexpr uint32_t idS = idesc_f32(128, kT / 2, false, E);   // one half: 64 keys
       constexpr uint32_t idO = idesc_f32(128, D, true, E);
       constexpr uint32_t kHi = desc_sw128_hi(1024);
       constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
+      constexpr uint32_t kHalfRows16 = (kT / 2) * 128 / 16;     // 64 rows of a 128-byte box, 16-byte units
       const uint32_t lq = desc_sw128_lo(sb + C::kOffRes, 16);
       const uint32_t ldo = desc_sw128_lo(sb + C::kOffRes + C::kTileBytes, 16);
-      bool ok = mbar_wait_w(bar(C::kBarRes), 0, s_abort, p.status);
+      // S = Q K^T and dP = dO V^T for the keys of half h of step j (rows on the
+      // lanes, 64 columns each)
+      auto scores = [&](int j, int h) {
+        const uint32_t sk = sb + C::kOffStages + (j % C::kStages) * C::kStageBytes;
+        const uint32_t lk = desc_sw128_lo(sk, 16) + (uint32_t)h * kHalfRows16;
+        const uint32_t lv = desc_sw128_lo(sk + C::kTileBytes, 16) + (uint32_t)h * kHalfRows16;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+          mma_ss_lh_w(tmem + C::kTmS + 64u * h, lq + off, kHi, lk + off, kHi, idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+          mma_ss_lh_w(tmem + C::kTmP + 64u * h, ldo + off, kHi, lv + off, kHi, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(bar(C::kBarS + h));
+      };
+      bool ok = mbar_wait_w(bar(C::kBarRes), 0, s_abort, p.status) &&
+                mbar_wait_w(bar(C::kBarFull + 0), 0, s_abort, p.status);
+      if (ok) {
+        tc_fence_after();
+        scores(0, 0);
+        scores(0, 1);
+      }
       for (int j = 0; j < n_steps && ok; ++j) {
         const int st = j % C::kStages;
-        const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-        if (!(ok = mbar_wait_w(bar(C::kBarFull + st), ph, s_abort, p.status))) break;
-        tc_fence_after();
-        const uint32_t sk = sb + C::kOffStages + st * C::kStageBytes;
-        const uint32_t lk = desc_sw128_lo(sk, 16), lv = desc_sw128_lo(sk + C::kTileBytes, 16);
-        // S = Q K^T and dP = dO V^T (rows on the lanes)
+        const uint32_t bk = desc_sw128_lo(sb + C::kOffStages + st * C::kStageBytes, C::kBoxBytes);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait_w(bar(C::kBarP + h), (uint32_t)j & 1u, s_abort, p.status))) break;
+          tc_fence_after();
+          // dQ += dS K over the 64 keys of half h: dS from tensor memory, K's
+          // tile as an MN-major operand
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-          mma_ss_lh_w(tmem + C::kTmS, lq + off, kHi, lk + off, kHi, idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kT / 32; ++kk)
+            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + 64u * h + (uint32_t)kk * 8u,
+                        bk + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
+                        (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          if (h == 1) mma_commit_w(bar(C::kBarEmpty + st));   // the stage's last reader
+          if (j + 1 < n_steps) {
+            if (h == 0) {
+              const int j1 = j + 1;
+              if (!(ok = mbar_wait_w(bar(C::kBarFull + j1 % C::kStages), (uint32_t)(j1 / C::kStages) & 1u,
+                                     s_abort, p.status)))
+                break;
+              tc_fence_after();
+            }
+            scores(j + 1, h);
+          }
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-          mma_ss_lh_w(tmem + C::kTmP, ldo + off, kHi, lv + off, kHi, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(bar(C::kBarS));
-        if (!(ok = mbar_wait_w(bar(C::kBarP), (uint32_t)j & 1u, s_abort, p.status))) break;
-        tc_fence_after();
-        // dQ += dS K: dS from tensor memory, K's tile as an MN-major operand
-        const uint32_t bk = desc_sw128_lo(sk, C::kBoxBytes);
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + (uint32_t)kk * 8u, bk + (uint32_t)kk * (16u * 128u >> 4),
-                      kHi, idO, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(bar(C::kBarEmpty + st));
       }
       mma_commit_w(bar(C::kBarDone));
       mma_commit_w(bar(C::kBarDrain));
@@ -518,28 +580,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // keys at or past `lim` are masked (ragged key range, causal diagonal)
     const int lim = p.causal ? min(p.N_k, row + p.kv_off + 1) : p.N_k;
     for (int j = 0; j < n_steps && ok; ++j) {
-      if (!(ok = mbar_wait_w(bar(C::kBarS), (uint32_t)j & 1u, s_abort, p.status))) break;
-      tc_fence_after();
-      const int key0 = j * kT;
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_w(bar(C::kBarS + h), (uint32_t)j & 1u, s_abort, p.status))) break;
+        tc_fence_after();
+        const int key0 = j * kT + 64 * h;
+        const uint32_t hS = tS + 64u * h, hP = tP + 64u * h;
 #pragma unroll 1
-      for (int cc = 0; cc < kT; cc += 32) {
-        float s[32], dp[32];
-        tmem_ld32(tS + (uint32_t)cc, s);
-        tmem_ld32(tP + (uint32_t)cc, dp);
-        tmem_wait_ld();
-        uint32_t pk[16];
+        for (int cc = 0; cc < kT / 2; cc += 32) {
+          float s[32], dp[32];
+          tmem_ld32(hS + (uint32_t)cc, s);
+          tmem_ld32(hP + (uint32_t)cc, dp);
+          tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int kx = key0 + cc + e;
-          float p0 = ex2_approx(s[e] * c - l2);
-          float p1 = ex2_approx(s[e + 1] * c - l2);
-          if (kx >= lim) p0 = 0.f;
-          if (kx + 1 >= lim) p1 = 0.f;
-          pk[e >> 1] = pack2<E>(p0 * (dp[e] - dd), p1 * (dp[e + 1] - dd));
+          for (int e = 0; e < 32; e += 2) {
+            const int kx = key0 + cc + e;
+            float p0 = ex2_approx(s[e] * c - l2);
+            float p1 = ex2_approx(s[e + 1] * c - l2);
+            if (kx >= lim) p0 = 0.f;
+            if (kx + 1 >= lim) p1 = 0.f;
+            pk[e >> 1] = pack2<E>(p0 * (dp[e] - dd), p1 * (dp[e + 1] - dd));
+          }
+          tmem_st16(hS + (uint32_t)(cc >> 1), pk);
         }
-        tmem_st16(tS + (uint32_t)(cc >> 1), pk);
+        bwd_publish(bar(C::kBarP + h));
       }
-      bwd_publish(bar(C::kBarP));
     }
     if (ok && n_steps > 0) {
       ok = mbar_wait_w(bar(C::kBarDone), 0, s_abort, p.status);
