@@ -7,22 +7,28 @@
 //   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
-// Three kernels on the caller's stream:
+// Two launches on the caller's stream:
 //  * fa_bwd_prep_kernel: per query row, lse2 = LSE log2(e) (+inf where the row
 //    sees no key, and on the padding rows of the last tile) and D, into arrays
 //    padded to whole 128-row tiles.
-//  * fa_bwd_dkdv_kernel: one CTA per (batch, KV head, block of 128 keys). K and
-//    V of the block stay in shared memory; the CTA walks the query tiles of
-//    every query head that reads the KV head (GQA sums them in place, no
-//    atomics). Keys are the TMEM lanes: S^T = K Q^T and dP^T = V dO^T (SS
-//    MMAs), then each thread (one key) turns its row into P^T and dS^T (BF16 or
-//    FP16, written back over its S^T / dP^T columns) and the MMA warp
-//    accumulates dV += P^T dO and dK += dS^T Q with A read from tensor memory.
-//  * fa_bwd_dq_kernel: one CTA per (batch, query head, 128-row tile); query rows
-//    are the TMEM lanes: S = Q K^T, dP = dO V^T, then dS, then dQ += dS K.
+//  * fa_bwd_kernel, whose CTAs take one of two roles (they share no data, so
+//    both run side by side in one grid, dK/dV CTAs first):
+//    - dK/dV: one CTA per (batch, KV head, block of 128 keys). K and V of the
+//      block stay in shared memory; the CTA walks the query tiles of every
+//      query head that reads the KV head (GQA sums them in place, no atomics).
+//      Keys are the TMEM lanes: S^T = K Q^T and dP^T = V dO^T (SS MMAs), then
+//      each thread (one key) turns its row into P^T and dS^T (BF16 or FP16,
+//      written back over its S^T / dP^T columns) and the MMA warp accumulates
+//      dV += P^T dO and dK += dS^T Q with A read from tensor memory.
+//    - dQ: one CTA per (batch, query head, 128-row tile); query rows are the
+//      TMEM lanes: S = Q K^T, dP = dO V^T, then dS, then dQ += dS K.
+//    Each step's score-shaped products run as two halves of 64 columns, and
+//    half h of the next step is issued right behind this half's accumulating
+//    products, so the element-wise pass over one half overlaps the tensor
+//    core's work on the other.
 // Every operand form is one the forward kernel uses: K-major SW128 tiles for
 // the score-shaped products, A from tensor memory with an MN-major B for the
-// accumulating ones. S and dP are computed twice (once per kernel): 14 N^2 d
+// accumulating ones. S and dP are computed twice (once per role): 14 N^2 d
 // FLOPs of work for the 10 N^2 d of the usual count, in exchange for no
 // atomic accumulation and deterministic results.
 #include "fa_internal.h"
@@ -175,10 +181,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* o, con
 
 // ---------------------------------------------------------------- dK, dV
 template <int D, Elem E>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const BwdParams p) {
+__device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                             const CUtensorMap& tmdO, const BwdParams& p, int blk) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bhk = blockIdx.x / p.n_kb;
-  const int kb = blockIdx.x - bhk * p.n_kb;
+  const int bhk = blk / p.n_kb;
+  const int kb = blk - bhk * p.n_kb;   // ascending: under a causal mask the first blocks are the longest
   const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
   const int j0 = kb * kT;
   // query tiles that see at least one key of the block
@@ -412,10 +416,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---------------------------------------------------------------- dQ
 template <int D, Elem E>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const BwdParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                           const CUtensorMap& tmdO, const BwdParams& p, int blk) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -425,8 +427,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bhq = blockIdx.x / p.n_qt;
-  const int t = blockIdx.x - bhq * p.n_qt;
+  const int bhq = blk / p.n_qt;
+  const int t = p.n_qt - 1 - (blk - bhq * p.n_qt);   // descending: under a causal mask the last tiles are the longest
   const int b = bhq / p.H_q, h = bhq - b * p.H_q;
   const int bhk = b * p.H_kv + h / p.G;
   const int q0 = t * kT;
@@ -625,6 +627,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// One launch for both halves of the work: CTAs [0, B*H_kv*n_kb) are dK/dV
+// CTAs, the rest dQ CTAs; the two roles share no data and run side by side,
+// longest work first within each role.
+template <int D, Elem E>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+  const int n_kv = p.B * p.H_kv * p.n_kb;
+  if ((int)blockIdx.x < n_kv)
+    bwd_dkdv_cta<D, E>(tmQ, tmK, tmV, tmdO, p, (int)blockIdx.x);
+  else
+    bwd_dq_cta<D, E>(tmQ, tmK, tmV, tmdO, p, (int)blockIdx.x - n_kv);
+}
+
 template <int D, Elem E>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
@@ -634,10 +651,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kLaunchSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchSmem);
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
@@ -646,11 +661,9 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                                 static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2,
                                 dsum, p.N_q, p.nq_pad, rows);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(fa_bwd_dkdv_kernel<D, E>, dim3((unsigned)(p.B * p.H_kv * p.n_kb)), dim3(kBwdThreads),
-                    C::kLaunchSmem, stream, tq, tk, tv, tdo, p);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(fa_bwd_dq_kernel<D, E>, dim3((unsigned)(p.B * p.H_q * p.n_qt)), dim3(kBwdThreads),
-                       C::kLaunchSmem, stream, tq, tk, tv, tdo, p);
+  const unsigned ctas = (unsigned)(p.B * p.H_kv * p.n_kb + p.B * p.H_q * p.n_qt);
+  return launch_kernel(fa_bwd_kernel<D, E>, dim3(ctas), dim3(kBwdThreads), C::kLaunchSmem, stream, tq, tk, tv,
+                       tdo, p);
 }
 
 bool aligned16p(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
@@ -704,8 +717,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* o, co
   p.scale = scale;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.status = status;
-  if ((long long)B * H_q * p.n_qt >= (1ll << 31) || (long long)B * H_kv * p.n_kb >= (1ll << 31))
-    return FA_ERR_INVALID_ARG;
+  if ((long long)B * H_q * p.n_qt + (long long)B * H_kv * p.n_kb >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, kT) ||
       !make_tmap_bf16_3d(&tdo, dout, d, N_q, (uint64_t)B * H_q, d, kT) ||

@@ -138,10 +138,10 @@ int fa_forward_host_packed(int n, const void* const* qkv, void* const* out, int 
  * and GQA conventions as fa_forward: dk and dv of a KV head sum over the query
  * heads that read it. The scores are recomputed tile by tile from q, k and the
  * saved lse, not stored ("Why is standard attention memory-bound...", Step 4).
- * Work: a per-row preprocessing kernel (D = rowsum(dout * o)), a dK/dV kernel
- * over key blocks and a dQ kernel over query tiles, on `stream`, with two
- * B*H_q*roundup(N_q, 128) FP32 arrays of stream-ordered workspace from libfa's
- * pool. Deterministic (no atomics). Pointers: device, 16-byte aligned; the
+ * Work: a per-row preprocessing kernel (D = rowsum(dout * o)), then one
+ * launch whose CTAs compute dK/dV over key blocks or dQ over query tiles, on
+ * `stream`, with two B*H_q*roundup(N_q, 128) FP32 arrays of stream-ordered
+ * workspace from libfa's pool. Deterministic (no atomics). Pointers: device, 16-byte aligned; the
  * outputs may not overlap any input or each other. When N_q or N_k is 0 the
  * gradients that exist are zero-filled. Returns FA_OK, FA_ERR_INVALID_ARG,
  * FA_ERR_UNSUPPORTED (d not 64/128), FA_ERR_NO_MEMORY or FA_ERR_CUDA. */
