@@ -51,6 +51,8 @@ KERNEL_SOURCES = {
                       "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
     "fa_decode_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
                          "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
+    "fa_bwd_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_bwd.cu",
+                      "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
 }
 
 
@@ -195,6 +197,18 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": reasons,
                 "source": src}
+
+
+def device_ids(props):
+    """(PCI bus id, UUID) of a device, as NVML names them (either may be None)."""
+    bus = getattr(props, "pci_bus_id", None)
+    bus_id = None
+    if bus is not None:
+        bus_id = (f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:"
+                  f"{getattr(props, 'pci_device_id', 0):02x}.0")
+    uuid = getattr(props, "uuid", None)
+    uuid = None if uuid is None else ("GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid))
+    return bus_id, uuid
 
 
 def to_device(torch, x, dev):
@@ -361,6 +375,160 @@ def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_
              "note": "the same steps as one request per call, nothing overlapped"})
 
 
+BWD_METRIC = "attention bwd TFLOP/s (10 N_q N_k d per head, halved when causal), % of GB300 roofline"
+
+
+def backward_flops(cfg) -> float:
+    """The backward's five products of 2 N_q N_k d each per query head (S, dP,
+    dV, dK, dQ): 2.5 times the forward's count, halved when causal."""
+    return 2.5 * W.flops_pages(cfg["B"], cfg["H_q"], cfg["N_q"], cfg["N_k"], cfg["d"], cfg["causal"])
+
+
+def cpu_oracle_backward(a, do, budget_s: float, max_n: int = 2048):
+    """The FP64 backward oracle on head 0 (and its KV head), cut to its first
+    ``max_n`` query rows and keys when longer, called again until ``budget_s``
+    has elapsed. Returns (FLOP/s, seconds, sample)."""
+    import oracle
+    n_q, n_k = min(a.N_q, max_n), min(a.N_k, max_n)
+    q, k, v, g = a.q[:1, :1, :n_q], a.k[:1, :1, :n_k], a.v[:1, :1, :n_k], do[:1, :1, :n_q]
+    t0 = time.perf_counter()
+    calls = 0
+    while calls == 0 or time.perf_counter() - t0 < budget_s:
+        oracle.attention_backward(q, k, v, g, causal=a.causal, scale=a.scale)
+        calls += 1
+    dt = time.perf_counter() - t0
+    flops = calls * 2.5 * W.flops_pages(1, 1, n_q, n_k, a.d, a.causal)
+    sample = (f"{calls} calls on head 0: {n_q} query rows x {n_k} keys (of {a.N_q} x {a.N_k} in each "
+              f"of {a.B * a.H_q} heads), FP64 materialised oracle, numpy/OpenBLAS")
+    return flops / dt, dt, sample
+
+
+def run_backward(args, rank, world, local, warmup):
+    """``--pass backward``: K fa_backward steps (prep kernel + one main launch)
+    back to back between two events, each on the next of several input sets
+    larger than L2 together; the forward's O and LSE come from fa_forward,
+    untimed. Prints one JSON line on rank 0."""
+    import torch
+    import exact_tiled_attention_forward_gb300 as fa
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    fa.lib()
+    cfg = dict(I.WORKLOADS[args.workload])
+    if cfg["N_q"] == 1:
+        raise SystemExit("--pass backward takes a prefill workload")
+    a = I.make_workload(args.workload, dtype=args.dtype)
+    do_h = I.grad_output(a, seed=0)
+    B, Hq, Hkv, Nq, Nk, d = a.shape_args
+    flops = backward_flops(cfg)
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    q, k, v, g = (to_device(torch, x, dev) for x in (a.q, a.k, a.v, do_h))
+    o, lse = fa.fa_forward(q, k, v, causal=a.causal, scale=a.scale)
+    set_bytes = (2 * q.numel() + 2 * k.numel() + o.numel() + g.numel()) * 2 + lse.numel() * 4
+    n_sets = min(256, max(2, -(-2 * l2_bytes // set_bytes)))
+    sets = []
+    for _ in range(n_sets):
+        sets.append(tuple(x.clone() for x in (q, k, v, o, lse, g)) +
+                    (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
+
+    def step(i):
+        qq, kk, vv, oo, ll, gg, dq, dk, dv = sets[i % n_sets]
+        fa.fa_backward(qq, kk, vv, oo, ll, gg, causal=a.causal, scale=a.scale, dq=dq, dk=dk, dv=dv)
+
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(*device_ids(props))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = R.slowest_rank_ms(e0.elapsed_time(e1), world, dev)
+    ms = total_ms / args.steps
+    value = R.whole_job_rate(flops / 1e12, args.steps, total_ms, world)
+    if fa.fa_device_status() != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait during the benchmark")
+
+    # end to end: every step copies q, k, v, o, lse, dO in from pinned host memory
+    # and dq, dk, dv back out, inside the timed region (nothing overlapped)
+    hin = [x.cpu().pin_memory() for x in (q, k, v, o, lse, g)]
+    hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, k, v)]
+    dins = [torch.empty_like(x) for x in (q, k, v, o, lse, g)]
+    douts = [torch.empty_like(x) for x in (q, k, v)]
+
+    def e2e_step():
+        for dx, hx in zip(dins, hin):
+            dx.copy_(hx, non_blocking=True)
+        fa.fa_backward(*dins, causal=a.causal, scale=a.scale, dq=douts[0], dk=douts[1], dv=douts[2])
+        for hx, dx in zip(hout, douts):
+            hx.copy_(dx, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = R.slowest_rank_ms(x0.elapsed_time(x1), world, dev)
+    h2d = sum(x.numel() * x.element_size() for x in hin)
+    d2h = sum(x.numel() * x.element_size() for x in hout)
+
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / 1e12 / (ms * 1e-3)
+    cpu = None
+    if args.cpu_budget > 0 and world == 1:
+        rate, dt, sample = cpu_oracle_backward(a, do_h, args.cpu_budget)
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)),
+               "kind": "oracle", "sample": f"{sample}, {dt:.1f} s"}
+    line = {
+        "metric": BWD_METRIC, "pass": "backward", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, **{k2: cfg[k2] for k2 in
+                   ("B", "H_q", "H_kv", "N_q", "N_k", "d", "causal")}, "scale": a.scale,
+                   "l2": (f"inputs larger than L2: {n_sets} copies of q, k, v, o, lse, dO (each with "
+                          f"its own dq, dk, dv) used in turn, {n_sets * set_bytes / 2**20:.0f} MiB "
+                          f"against {l2_bytes / 2**20:.0f} MiB of L2; steps back to back"),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(args.workload, "fa_bwd_kernel"),
+                     "peak_source": f"{peak_src} (burst)", "algorithmic_per_launch": flops,
+                     "kernel": ("fa_bwd_kernel, timed together with fa_bwd_prep_kernel (the "
+                                "step's other launch): a lower bound on the main kernel's rate")},
+        "cpu_baseline": cpu,
+        "e2e": {"value": R.whole_job_rate(flops / 1e12, args.steps, e2e_ms, world), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+                "note": "fa_backward with torch copies from and to pinned host memory, nothing overlapped"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -374,12 +542,19 @@ def main():
                     help="timed steps of the decode workload reported beside the prefill line")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of host time for the cpu_baseline leg (0 disables it)")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                    help="backward: time fa_backward on the workload instead (fused impl only)")
     args = ap.parse_args()
     if args.impl == "naive" and args.dtype != "bf16":
         ap.error("the unfused baseline is BF16 only")
     warmup = max(3, args.warmup)
 
     rank, world, local = R.replica_env()
+    if args.which == "backward":
+        if args.impl != "fused":
+            ap.error("--pass backward times the fused library path only")
+        run_backward(args, rank, world, local, warmup)
+        return
     cfg, a_flops, a_bytes, decode_cfg = workload_config(args.workload)
     unit = "GB/s" if decode_cfg else "TFLOP/s"
     work_per_step = (a_bytes / 1e9) if decode_cfg else (a_flops / 1e12)
@@ -470,14 +645,7 @@ def main():
         step(i)
     barrier()
 
-    bus = getattr(props, "pci_bus_id", None)
-    bus_id = None
-    if bus is not None:
-        bus_id = (f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:"
-                  f"{getattr(props, 'pci_device_id', 0):02x}.0")
-    uuid = getattr(props, "uuid", None)
-    uuid = None if uuid is None else ("GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid))
-    sampler = ClockSampler(bus_id, uuid)
+    sampler = ClockSampler(*device_ids(props))
     sampler.start()
     # ---- timed region: K steps back to back between two events on the launching
     # stream, each step on the next input set (inputs larger than L2)
