@@ -40,9 +40,12 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 256;   // warps 0-3 element-wise (one TMEM lane each), 4 TMA, 5 MMA, 6-7 idle
-constexpr int kBwdWarpProducer = 4;
-constexpr int kBwdWarpMma = 5;
+// warps 0-7 element-wise: two warpgroups on the same 128 TMEM lanes, warpgroup g
+// taking columns [32g, 32g+32) of every 64-column half; warp 8 TMA, warp 9 MMA
+constexpr int kBwdThreads = 320;
+constexpr int kBwdEwThreads = 256;
+constexpr int kBwdWarpProducer = 8;
+constexpr int kBwdWarpMma = 9;
 constexpr int kT = 128;            // query rows per tile = keys per block
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -86,10 +89,11 @@ struct BwdCfg {
   static constexpr int kLaunchSmem = kSmemBytes < 116 * 1024 ? 116 * 1024 : kSmemBytes;
   static_assert(kLaunchSmem <= 227 * 1024, "shared memory");
   static constexpr uint32_t kTmemCols = 512;
-  // tensor memory: [0,128) S or S^T, [128,256) dP or dP^T, each as two halves
-  // of 64 columns (P / P^T packed over the first 32 columns of its S half,
-  // dS / dS^T over the first 32 of its dP half); [256,256+D) dV or dQ,
-  // [384,384+D) dK
+  // tensor memory: [0,128) S or S^T, [128,256) dP or dP^T, each as four
+  // chunks of 32 columns (two per 64-column half); the 16-bit P / P^T or dS /
+  // dS^T of a chunk's 32 rows or keys is packed over the chunk's own first 16
+  // columns (so neither warpgroup writes a column the other still reads);
+  // [256,256+D) dV or dQ, [384,384+D) dK
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmA = 256, kTmB = 384;
 };
 
@@ -100,6 +104,12 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Tensor-memory column of the packed 16-bit operand for K-step kk (16 rows or
+// keys) of half h: chunk kk / 2 of the half, its first 16 columns.
+__device__ __forceinline__ uint32_t packed_col(int h, int kk) {
+  return 64u * (uint32_t)h + (uint32_t)(kk >> 1) * 32u + (uint32_t)(kk & 1) * 8u;
 }
 
 __device__ __forceinline__ void bwd_publish(uint32_t bar) {
@@ -124,10 +134,12 @@ __device__ __forceinline__ float widen16(uint16_t bits) {
 // memory as 16-bit values times `mul`; `zero` writes zeros instead (no MMA ran).
 // Called by every lane of the warp with warp-uniform `zero` (the tensor-memory
 // load is a warp-collective instruction); only lanes with `valid` store.
+// Columns [c0, c1), multiples of 32.
 template <int D, Elem E>
-__device__ __forceinline__ void store_row(uint32_t t_row, uint16_t* dst, float mul, bool zero, bool valid) {
+__device__ __forceinline__ void store_row(uint32_t t_row, uint16_t* dst, float mul, bool zero, bool valid,
+                                          int c0 = 0, int c1 = D) {
 #pragma unroll 1
-  for (int cc = 0; cc < D; cc += 32) {
+  for (int cc = c0; cc < c1; cc += 32) {
     float v[32];
     if (zero) {
 #pragma unroll
@@ -213,7 +225,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kBarS + h), 1);
-      mbar_init(bar(C::kBarP + h), 128);
+      mbar_init(bar(C::kBarP + h), kBwdEwThreads);
     }
     mbar_init(bar(C::kBarDone), 1);
     mbar_init(bar(C::kBarDrain), 1);
@@ -316,12 +328,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
           // operand; K-steps of 16 rows
 #pragma unroll
           for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + 64u * h + (uint32_t)kk * 8u,
+            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + packed_col(h, kk),
                         bdo + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
                         (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_lh_w(tmem + C::kTmB, tmem + C::kTmP + 64u * h + (uint32_t)kk * 8u,
+            mma_ts_lh_w(tmem + C::kTmB, tmem + C::kTmP + packed_col(h, kk),
                         bq + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
                         (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
           if (h == 1) mma_commit_w(bar(C::kBarEmpty + st));   // the stage's last reader
@@ -344,11 +356,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       bwd_drain_wait(bar(C::kBarDrain), 0, p.status);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ---- element-wise: this thread is key k of the block (TMEM lane k)
-    const int k = warp * 32 + lane;
+  } else if (warp < 8) {
+    // ---- element-wise: this thread is key k of the block (TMEM lane k), in
+    // warpgroup grp, which takes the 32-row chunk grp of every half
+    const int grp = warp >> 2;
+    const int k = (warp & 3) * 32 + lane;
     const int key = j0 + k;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::kTmS, tP = tmem + lane_base + C::kTmP;
     const float c = p.c;
     bool ok = true;
@@ -368,29 +382,25 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         if (h == 0 &&
             !(ok = mbar_wait_w(bar(C::kBarFull + st), (uint32_t)(i / C::kStages) & 1u, s_abort, p.status)))
           break;
-        const uint32_t hS = tS + 64u * h, hP = tP + 64u * h;
-#pragma unroll 1
-        for (int cc = 0; cc < kT / 2; cc += 32) {
-          float s[32], dp[32];
-          tmem_ld32(hS + (uint32_t)cc, s);
-          tmem_ld32(hP + (uint32_t)cc, dp);
-          tmem_wait_ld();
-          uint32_t pk[16], dk2[16];
+        const uint32_t cc = 64u * h + 32u * grp;   // this warpgroup's 32 columns = rows
+        float s[32], dp[32];
+        tmem_ld32(tS + cc, s);
+        tmem_ld32(tP + cc, dp);
+        tmem_wait_ld();
+        uint32_t pk[16], dk2[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int r = 64 * h + cc + e;
-            float p0 = ex2_approx(s[e] * c - vl[r]);
-            float p1 = ex2_approx(s[e + 1] * c - vl[r + 1]);
-            if (r < r_min) p0 = 0.f;
-            if (r + 1 < r_min) p1 = 0.f;
-            pk[e >> 1] = pack2<E>(p0, p1);
-            dk2[e >> 1] = pack2<E>(p0 * (dp[e] - vd[r]), p1 * (dp[e + 1] - vd[r + 1]));
-          }
-          // over columns already read: P^T / dS^T of the half's rows cc .. cc+31
-          // in its columns cc/2 ..
-          tmem_st16(hS + (uint32_t)(cc >> 1), pk);
-          tmem_st16(hP + (uint32_t)(cc >> 1), dk2);
+        for (int e = 0; e < 32; e += 2) {
+          const int r = (int)cc + e;
+          float p0 = ex2_approx(s[e] * c - vl[r]);
+          float p1 = ex2_approx(s[e + 1] * c - vl[r + 1]);
+          if (r < r_min) p0 = 0.f;
+          if (r + 1 < r_min) p1 = 0.f;
+          pk[e >> 1] = pack2<E>(p0, p1);
+          dk2[e >> 1] = pack2<E>(p0 * (dp[e] - vd[r]), p1 * (dp[e + 1] - vd[r + 1]));
         }
+        // P^T / dS^T of the chunk's 32 rows over its own first 16 columns (read above)
+        tmem_st16(tS + cc, pk);
+        tmem_st16(tP + cc, dk2);
         bwd_publish(bar(C::kBarP + h));
       }
     }
@@ -401,9 +411,11 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     if (ok) {   // warp-uniform; keys past N_k (a ragged last block) load but do not store
       const bool valid = key < p.N_k;
       const size_t row = ((size_t)bhk * p.N_k + (valid ? key : 0)) * D;
-      store_row<D, E>(tmem + lane_base + C::kTmA, static_cast<uint16_t*>(p.dv) + row, 1.f, n_steps == 0, valid);
-      store_row<D, E>(tmem + lane_base + C::kTmB, static_cast<uint16_t*>(p.dk) + row, p.scale, n_steps == 0,
-                      valid);
+      if (grp == 0)   // warpgroup 0 writes dV, warpgroup 1 dK
+        store_row<D, E>(tmem + lane_base + C::kTmA, static_cast<uint16_t*>(p.dv) + row, 1.f, n_steps == 0, valid);
+      else
+        store_row<D, E>(tmem + lane_base + C::kTmB, static_cast<uint16_t*>(p.dk) + row, p.scale, n_steps == 0,
+                        valid);
     }
   }
   tc_fence_before();
@@ -447,7 +459,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kBarS + h), 1);
-      mbar_init(bar(C::kBarP + h), 128);
+      mbar_init(bar(C::kBarP + h), kBwdEwThreads);
     }
     mbar_init(bar(C::kBarDone), 1);
     mbar_init(bar(C::kBarDrain), 1);
@@ -543,7 +555,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
           // tile as an MN-major operand
 #pragma unroll
           for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + 64u * h + (uint32_t)kk * 8u,
+            mma_ts_lh_w(tmem + C::kTmA, tmem + C::kTmS + packed_col(h, kk),
                         bk + (uint32_t)h * kHalfRows16 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO,
                         (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
           if (h == 1) mma_commit_w(bar(C::kBarEmpty + st));   // the stage's last reader
@@ -564,11 +576,13 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       bwd_drain_wait(bar(C::kBarDrain), 0, p.status);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ---- element-wise: this thread is query row r of the tile (TMEM lane r)
-    const int r = warp * 32 + lane;
+  } else if (warp < 8) {
+    // ---- element-wise: this thread is query row r of the tile (TMEM lane r),
+    // in warpgroup grp, which takes the 32-key chunk grp of every half
+    const int grp = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int row = q0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::kTmS, tP = tmem + lane_base + C::kTmP;
     const float c = p.c;
     bool ok = true;
@@ -585,26 +599,24 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       for (int h = 0; h < 2; ++h) {
         if (!(ok = mbar_wait_w(bar(C::kBarS + h), (uint32_t)j & 1u, s_abort, p.status))) break;
         tc_fence_after();
-        const int key0 = j * kT + 64 * h;
-        const uint32_t hS = tS + 64u * h, hP = tP + 64u * h;
-#pragma unroll 1
-        for (int cc = 0; cc < kT / 2; cc += 32) {
-          float s[32], dp[32];
-          tmem_ld32(hS + (uint32_t)cc, s);
-          tmem_ld32(hP + (uint32_t)cc, dp);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        const uint32_t cc = 64u * h + 32u * grp;   // this warpgroup's 32 columns = keys
+        const int key0 = j * kT + (int)cc;
+        float s[32], dp[32];
+        tmem_ld32(tS + cc, s);
+        tmem_ld32(tP + cc, dp);
+        tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int kx = key0 + cc + e;
-            float p0 = ex2_approx(s[e] * c - l2);
-            float p1 = ex2_approx(s[e + 1] * c - l2);
-            if (kx >= lim) p0 = 0.f;
-            if (kx + 1 >= lim) p1 = 0.f;
-            pk[e >> 1] = pack2<E>(p0 * (dp[e] - dd), p1 * (dp[e + 1] - dd));
-          }
-          tmem_st16(hS + (uint32_t)(cc >> 1), pk);
+        for (int e = 0; e < 32; e += 2) {
+          const int kx = key0 + e;
+          float p0 = ex2_approx(s[e] * c - l2);
+          float p1 = ex2_approx(s[e + 1] * c - l2);
+          if (kx >= lim) p0 = 0.f;
+          if (kx + 1 >= lim) p1 = 0.f;
+          pk[e >> 1] = pack2<E>(p0 * (dp[e] - dd), p1 * (dp[e + 1] - dd));
         }
+        // dS of the chunk's 32 keys over its own first 16 columns (read above)
+        tmem_st16(tS + cc, pk);
         bwd_publish(bar(C::kBarP + h));
       }
     }
@@ -613,10 +625,10 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       tc_fence_after();
     }
     if (ok) {   // warp-uniform; rows past N_q (a ragged last tile) load but do not store
-      const bool valid = row < p.N_q;
+      const bool valid = row < p.N_q;   // warpgroup g writes columns [g D/2, (g+1) D/2)
       store_row<D, E>(tmem + lane_base + C::kTmA,
                       static_cast<uint16_t*>(p.dq) + ((size_t)bhq * p.N_q + (valid ? row : 0)) * D, p.scale,
-                      n_steps == 0, valid);
+                      n_steps == 0, valid, grp * (D / 2), (grp + 1) * (D / 2));
     }
   }
   tc_fence_before();
