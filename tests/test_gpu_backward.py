@@ -188,3 +188,39 @@ def test_backward_empty(fa):
     dq, dk, dv = fa.fa_backward(q, k, k, o, lse, q.clone(), dq=dq)
     torch.cuda.synchronize()
     assert torch.all(dq == 0) and dk.numel() == 0 and dv.numel() == 0
+
+
+FULL = ["one_head_n8192_d128", "h32_n4096_d128", "h32_n4096_d128_causal", "h32_n16384_d128_causal_krows"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_backward_full_size(fa, name):
+    # The workloads `bench.py --pass backward` times, whole, in the same launch
+    # configuration. Heads are independent, so the sampled KV heads (first and
+    # last; the last only past N = 8192, where one FP64 head is ~10 GB of
+    # scores) and their query heads take O and LSE from the oracle and are
+    # checked element by element; the other heads take them from libfa's forward.
+    import torch
+    a = I.make_workload(name)
+    do = I.grad_output(a, seed=0)
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    o, lse = fa.fa_forward(q, k, v, causal=a.causal, scale=a.scale)
+    g = a.H_q // a.H_kv
+    subs = []
+    for hk in ([a.H_kv - 1] if a.N_q > 8192 else sorted({0, a.H_kv - 1})):
+        hs = slice(hk * g, (hk + 1) * g)
+        sub = I.AttentionInputs(a.q[:, hs], a.k[:, hk:hk + 1], a.v[:, hk:hk + 1], a.B, g, 1, a.N_q, a.N_k,
+                                a.d, a.causal, a.scale, a.dtype)
+        o16, lse32 = _forward_inputs(sub)
+        o[:, hs] = to_dev(o16)
+        lse[:, hs] = torch.from_numpy(np.ascontiguousarray(lse32)).cuda()
+        subs.append((hk, hs, sub))
+    torch.cuda.synchronize()
+    dq, dk, dv = fa.fa_backward(q, k, v, o, lse, to_dev(do), causal=a.causal, scale=a.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    for hk, hs, sub in subs:
+        got = [dq[:, hs].float().cpu().numpy().astype(np.float64),
+               dk[:, hk:hk + 1].float().cpu().numpy().astype(np.float64),
+               dv[:, hk:hk + 1].float().cpu().numpy().astype(np.float64)]
+        check_gradients(sub, do[:, hs], got)
