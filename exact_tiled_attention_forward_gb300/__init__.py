@@ -58,6 +58,7 @@ _SIGNATURES = {
                                [_c_float, _c_int, _vp]),
     "fa_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_backward": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _c_int, _vp]),
+    "fa_decode_paged": (_c_int, [_vp] * 7 + [_c_int] * 8 + [_c_float, _c_int, _vp]),
     "fa_naive_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 +
                          [_c_float, _vp, _c_size, _vp]),
     "fa_naive_workspace_bytes": (_c_size, [_c_int] * 4),
@@ -272,6 +273,40 @@ def fa_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None =
                            _stream_ptr(stream))
     _check(st, "fa_backward")
     return dq, dk, dv
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, causal: bool = False,
+                    scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Decode over a paged K/V cache. q ``[B, H_q, N_q, d]``; k_cache, v_cache
+    ``[num_pages, H_kv, 128, d]`` (BF16 or FP16, q's type); block_table int32
+    ``[B, max_pages]``; seqlens_k int32 ``[B]``; all on the device. Returns
+    ``(o, lse)`` as ``fa_forward`` does."""
+    import torch
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q is {dtype}, expected torch.bfloat16 or torch.float16")
+    _check_dtypes(dtype, q, k_cache, v_cache, out, lse)
+    for name, t in (("block_table", block_table), ("seqlens_k", seqlens_k)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} is {t.dtype}, expected torch.int32")
+    B, H_q, N_q, d = q.shape
+    num_pages, H_kv, page, dk = k_cache.shape
+    if page != 128 or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache must be [num_pages, H_kv, 128, d] with q's d")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seqlens_k.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seqlens_k [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seqlens_k),
+                               _ptr(out), _ptr(lse), B, H_q, H_kv, N_q, num_pages, block_table.shape[1], d,
+                               int(bool(causal)), float(scale),
+                               FA_DTYPE_FP16 if dtype == torch.float16 else FA_DTYPE_BF16, _stream_ptr(stream))
+    _check(st, "fa_decode_paged")
+    return out, lse
 
 
 def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None, out=None,

@@ -111,7 +111,15 @@ __global__ void __launch_bounds__(kDecThreads)
   const int bhk = blockIdx.x / p.n_parts;
   const int b = bhk / p.H_kv, hk = bhk - b * p.H_kv;
   const int c_begin = part * p.cpc;
-  const int nc = min(p.n_chunks, c_begin + p.cpc) - c_begin;   // >= 1
+  // keys of this sequence (paged K/V: each sequence has its own length)
+  int n_k = p.N_k, kv_off = p.kv_off, n_chunks = p.n_chunks;
+  if (p.paged) {
+    n_k = min(max(__ldg(p.seqlens + b), 0), p.max_pages * kDecKeys);
+    kv_off = n_k - p.N_q;
+    n_chunks = (n_k + kDecKeys - 1) / kDecKeys;
+  }
+  // chunks of this run; 0 only for a paged sequence shorter than the run's start
+  const int nc = max(0, min(n_chunks, c_begin + p.cpc) - c_begin);
 
   if (threadIdx.x == 0) {
     mbar_init(barK, 1);
@@ -121,11 +129,18 @@ __global__ void __launch_bounds__(kDecThreads)
   __syncthreads();
   auto load = [&](uint32_t bar, uint32_t off, const CUtensorMap* tm, int chunk) {
     mbar_arrive_expect_tx(bar, C::kTileBytes);
+    // contiguous: rows chunk*128.. of (batch, KV head) slab bhk; paged: the
+    // whole 128-row slab (page, KV head) (an index outside the cache reads zeros)
+    int row = chunk * kDecKeys, slab = bhk;
+    if (p.paged) {
+      row = 0;
+      slab = __ldg(p.block_table + (size_t)b * p.max_pages + chunk) * p.H_kv + hk;
+    }
 #pragma unroll
     for (int bx = 0; bx < C::kBoxes; ++bx)
-      tma_load_3d(sb + off + bx * C::kBoxBytes, tm, bar, bx * 64, chunk * kDecKeys, bhk);
+      tma_load_3d(sb + off + bx * C::kBoxBytes, tm, bar, bx * 64, row, slab);
   };
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && nc > 0) {
     load(barK, C::kOffK, &tmK, c_begin);
     load(barV, C::kOffV, &tmV, c_begin);
   }
@@ -164,7 +179,7 @@ __global__ void __launch_bounds__(kDecThreads)
   for (int dn = 0; dn < D / 8; ++dn)
 #pragma unroll
     for (int e = 0; e < 4; ++e) oacc[dn][e] = 0.f;
-  int k_loads = 1, v_loads = 1;   // loads issued (thread 0), for the drain on failure
+  int k_loads = nc > 0 ? 1 : 0, v_loads = k_loads;   // loads issued (thread 0), for the drain on failure
   bool ok = true;
   for (int ci = 0; ci < nc; ++ci) {
     const int key0 = (c_begin + ci) * kDecKeys;
@@ -202,8 +217,8 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int u = 0; u < 2; ++u) {
       const int m = g + 8 * u;
       const int i = (m < p.R) ? m % p.N_q : 0;
-      int lim = p.N_k - key0;                                  // keys of this chunk that exist
-      if (p.causal) lim = min(lim, i + p.kv_off + 1 - key0);   // ... and that row i may see
+      int lim = n_k - key0;                                    // keys of this chunk that exist
+      if (p.causal) lim = min(lim, i + kv_off + 1 - key0);     // ... and that row i may see
       if (m >= p.R) lim = 0;
       float mx = -INFINITY;
 #pragma unroll

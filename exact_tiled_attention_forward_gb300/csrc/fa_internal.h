@@ -84,6 +84,14 @@ struct DecParams {
   float* part_o;     // fp32 [B*H_kv][n_parts][R][d]
   float* part_ml;    // fp32 [B*H_kv][n_parts][R][2]
   int* status;
+  // paged K/V (paged = 1): K and V are [num_pages][H_kv][128][d]; sequence b's
+  // chunk c is page block_table[b * max_pages + c]; its key count is
+  // seqlens[b] (clamped to [0, max_pages * 128]); N_k and n_chunks are then
+  // the maxima (max_pages * 128, max_pages)
+  int paged;
+  int max_pages;
+  const int* block_table;
+  const int* seqlens;
 };
 size_t decode_part_bytes(int B, int H_kv, int R, int n_parts, int d);
 // How the decode kernel cuts `heads` = B * H_kv KV heads of n_chunks chunks each.
@@ -146,6 +154,7 @@ inline cudaError_t launch_kernel(void (*kernel)(K...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
 }
 int num_sms();
+bool cluster_merge_enabled();   // in-cluster merge of partials unless FA_CLUSTER_MERGE=0
 extern thread_local int g_last_cuda_error;
 
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.

@@ -33,7 +33,7 @@ GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_ROWS, STREAM_DO = 1, 2, 3, 4, 5
+STREAM_Q, STREAM_K, STREAM_V, STREAM_ROWS, STREAM_DO, STREAM_PAGES = 1, 2, 3, 4, 5, 6
 
 _CHUNK = 1 << 22  # elements generated per numpy pass (bounds temporaries)
 
@@ -184,6 +184,77 @@ def grad_output(a: AttentionInputs, seed: int = 0) -> np.ndarray:
     """dO for a backward pass of `a`: N(0, 1) in a's storage type, shaped like O."""
     shape = (a.B, a.H_q, a.N_q, a.d)
     return normal_f16(seed, STREAM_DO, shape) if a.dtype == "f16" else normal_bf16(seed, STREAM_DO, shape)
+
+
+PAGE_KEYS = 128   # keys per page of a paged K/V cache
+
+
+@dataclasses.dataclass
+class PagedInputs:
+    """A decode problem whose K/V cache is paged. ``q`` ``[B][H_q][N_q][d]``;
+    ``k_cache``, ``v_cache`` ``[num_pages][H_kv][128][d]``; ``block_table``
+    int32 ``[B][max_pages]`` (key j of sequence b is row j % 128 of page
+    ``block_table[b][j // 128]``); ``seqlens`` int32 ``[B]``. Element storage
+    as in ``AttentionInputs``."""
+    q: np.ndarray
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    block_table: np.ndarray
+    seqlens: np.ndarray
+    B: int
+    H_q: int
+    H_kv: int
+    N_q: int
+    d: int
+    causal: bool
+    scale: float
+    dtype: str = "bf16"
+
+
+def make_paged(B: int, H_q: int, H_kv: int, N_q: int, seqlens, d: int, *, causal: bool = False,
+               scale: float | None = None, seed: int = 0, spare_pages: int = 3, max_pages: int | None = None,
+               k_row_frac: float = 0.0, dtype: str = "bf16") -> PagedInputs:
+    """Q, K, V drawn as ``make_inputs`` draws them (K and V for
+    ``max_pages * 128`` keys per sequence), then K/V laid out in pages.
+
+    Sequence b keeps its first ``ceil(seqlens[b] / 128)`` key blocks, each in a
+    page of its own; pages are numbered in a seeded random order, with
+    ``spare_pages`` extra pages (random data no sequence owns) among them. The
+    keys of a sequence's last page past its length keep their drawn values, and
+    block-table entries past a sequence's last page hold seeded page numbers:
+    neither may change a result. ``max_pages`` defaults to the longest
+    sequence's page count."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    assert seqlens.shape == (B,) and (seqlens >= 0).all()
+    used = (seqlens + PAGE_KEYS - 1) // PAGE_KEYS
+    if max_pages is None:
+        max_pages = max(1, int(used.max()) if B else 1)
+    assert (used <= max_pages).all()
+    a = make_inputs(B, H_q, H_kv, N_q, max_pages * PAGE_KEYS, d, causal=causal, scale=scale, seed=seed,
+                    k_row_frac=k_row_frac, dtype=dtype)
+    num_pages = int(used.sum()) + spare_pages
+    order = np.argsort(uniform_u64(seed, STREAM_PAGES, 0, max(num_pages, 1)), kind="stable")[:num_pages]
+    k_cache = np.empty((num_pages, H_kv, PAGE_KEYS, d), dtype=a.k.dtype)
+    v_cache = np.empty_like(k_cache)
+    table = (uniform_u64(seed, STREAM_PAGES, num_pages, B * max_pages) % np.uint64(max(num_pages, 1)))
+    table = table.astype(np.int32).reshape(B, max_pages)
+    slot = 0
+    for b in range(B):
+        for j in range(int(used[b])):
+            page = int(order[slot])
+            slot += 1
+            table[b, j] = page
+            k_cache[page] = a.k[b, :, j * PAGE_KEYS:(j + 1) * PAGE_KEYS]
+            v_cache[page] = a.v[b, :, j * PAGE_KEYS:(j + 1) * PAGE_KEYS]
+    # the spare pages: data of other seeded draws
+    spare = order[slot:]
+    if len(spare):
+        draw = normal_f16 if dtype == "f16" else normal_bf16
+        fill = draw(seed + 1, STREAM_K, (len(spare), H_kv, PAGE_KEYS, d))
+        k_cache[spare] = fill
+        v_cache[spare] = fill[::-1]
+    return PagedInputs(a.q, k_cache, v_cache, table, seqlens.astype(np.int32), B, H_q, H_kv, N_q, d,
+                       a.causal, a.scale, dtype)
 
 
 # The five workloads the method is measured on (batch, heads, lengths, head dim,

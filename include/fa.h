@@ -149,6 +149,32 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
                 const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N_q,
                 int N_k, int d, int causal, float scale, int dtype, void* stream);
 
+/* Decode attention over a paged K/V cache: for each sequence b, the N_q
+ * query rows of q (layout as fa_forward) attend to that sequence's first
+ * seqlens_k[b] keys, in order, exactly as fa_forward would over the same keys
+ * stored contiguously (same scale, causal and GQA conventions; a sequence of
+ * length 0, or a causal row that sees no key, gets O = 0 and LSE = -inf).
+ * Decode is reading K and V once per KV head ("FlashAttention HBM bytes, one
+ * head, 8K", "What interviewers probe next"); the pages describe no cache
+ * layout, so this layout is the library's own:
+ *  - k_cache, v_cache: element type dtype, [num_pages][H_kv][128][d]: a page
+ *    holds 128 consecutive keys of one sequence for every KV head; device,
+ *    16-byte aligned.
+ *  - block_table: int32 [B][max_pages], device: key j of sequence b is row
+ *    j % 128 of page block_table[b][j / 128]. Entries past a sequence's last
+ *    page are not read; every entry that is read must lie in [0, num_pages)
+ *    (an entry outside it reads as zeros, it does not fault).
+ *  - seqlens_k: int32 [B], device; values are clamped to [0, max_pages * 128].
+ *  - o: dtype [B][H_q][N_q][d]; lse: FP32 [B][H_q][N_q] or NULL.
+ * Rows per KV head, (H_q / H_kv) * N_q, must be at most 16 (the decode
+ * kernel's tile), else FA_ERR_UNSUPPORTED. Workspace for the partials of long
+ * sequences comes from libfa's stream-ordered pool (none when they are merged
+ * inside a thread-block cluster). Returns FA_OK, FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED, FA_ERR_NO_MEMORY or FA_ERR_CUDA. */
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                    const int* seqlens_k, void* o, float* lse, int B, int H_q, int H_kv, int N_q,
+                    int num_pages, int max_pages, int d, int causal, float scale, int dtype, void* stream);
+
 /* fa_forward without any device-memory allocation. (The pages have no
  * counterpart: this exists for callers, not for the method.)
  * For callers that cannot allocate device memory on this path: a serving loop

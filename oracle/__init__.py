@@ -17,6 +17,8 @@ Contents
 ``traffic``    the pages' analytic HBM byte and FLOP counts.
 ``backward``   FP64 gradients dQ, dK, dV of the definition (chain rule, pinned by
                finite differences of the forward).
+``paged``      decode over a paged K/V cache: each sequence's keys read out of
+               its pages in order, then the definition.
 
 Every function names the page and section it follows. Each is pinned in
 ``tests/test_oracle_*.py`` against values the pages print, closed forms and
@@ -35,3 +37,4 @@ from .attention import (  # noqa: F401
 )
 from . import traffic  # noqa: F401
 from .backward import attention_backward, backward_error_terms, forward_loss  # noqa: F401
+from .paged import gather_sequence, paged_attention_reference  # noqa: F401

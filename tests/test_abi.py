@@ -26,7 +26,7 @@ def lib():
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
     assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_host", "fa_forward_host_packed",
-                          "fa_backward",
+                          "fa_backward", "fa_decode_paged",
                           "fa_forward_noalloc",
                           "fa_naive_forward",
                           "fa_naive_workspace_bytes", "fa_forward_plan", "fa_selftest_wait_timeout",
@@ -231,3 +231,32 @@ def test_backward_rejects(lib):
     assert call(dq=0x10000000 + 64) == fa.FA_ERR_INVALID_ARG       # dq overlaps q
     assert call(dk=0x70000000) == fa.FA_ERR_INVALID_ARG            # dk overlaps dq
     assert call(dv=0x30000000) == fa.FA_ERR_INVALID_ARG            # dv aliases v
+
+
+def test_decode_paged_rejects(lib):
+    f = lib.fa_decode_paged
+    # q, k_cache, v_cache, block_table, seqlens, o, lse
+    ok_ptrs = [0x10000000 * (i + 1) for i in range(7)]           # disjoint, 16-byte aligned
+    names_p = ["q", "kc", "vc", "table", "lens", "o", "lse"]
+    names_a = ["B", "Hq", "Hkv", "Nq", "pages", "max_pages", "d", "causal", "scale", "dtype"]
+    args = (2, 8, 2, 1, 16, 4, 128, 0, 0.1, 0, None)
+
+    def call(**kw):
+        p = [kw.get(n, ok_ptrs[i]) for i, n in enumerate(names_p)]
+        a = [kw.get(n, args[i]) for i, n in enumerate(names_a)] + [None]
+        return f(*p, *a)
+    assert call(Hq=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(Nq=5) == fa.FA_ERR_UNSUPPORTED          # 4 heads x 5 rows per KV head > 16
+    assert call(scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=2) == fa.FA_ERR_INVALID_ARG
+    assert call(pages=0) == fa.FA_ERR_INVALID_ARG
+    assert call(max_pages=0) == fa.FA_ERR_INVALID_ARG
+    assert call(table=0) == fa.FA_ERR_INVALID_ARG
+    assert call(lens=0x50000002) == fa.FA_ERR_INVALID_ARG      # misaligned int32
+    assert call(kc=0x20000008) == fa.FA_ERR_INVALID_ARG        # misaligned cache
+    assert call(o=0x10000000 + 256) == fa.FA_ERR_INVALID_ARG   # o overlaps q
+    assert call(lse=0x40000000) == fa.FA_ERR_INVALID_ARG       # lse overlaps the block table
+    assert call(pages=1 << 29, Hkv=8, Hq=8) == fa.FA_ERR_INVALID_ARG   # page x head index past 31 bits
+    assert call(B=0) == fa.FA_OK                                # nothing to do
+
