@@ -529,6 +529,165 @@ def run_backward(args, rank, world, local, warmup):
         torch.distributed.destroy_process_group()
 
 
+PAGED_METRIC = "paged decode HBM GB/s (K/V read once per KV head), % of GB300 roofline"
+
+
+def run_paged(args, rank, world, local, warmup):
+    """``--pass paged``: the decode workload (batch 16, 32 query / 8 KV heads,
+    8192 keys, d = 128) with its K/V cache in shuffled 128-key pages, through
+    fa_decode_paged. Two cache sets (537 MB each) used in turn, K steps back to
+    back between two events; the same steps one at a time after an L2 flush;
+    end to end with every input copied in from pinned host memory and O, LSE
+    copied out; the contiguous layout through fa_forward beside it. One JSON
+    line on rank 0."""
+    import torch
+    import exact_tiled_attention_forward_gb300 as fa
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    fa.lib()
+    cfg = dict(I.WORKLOADS[DECODE_WORKLOAD])
+    B, Hq, Hkv, Nq, Nk, d = (cfg[x] for x in ("B", "H_q", "H_kv", "N_q", "N_k", "d"))
+    pin = I.make_paged(B, Hq, Hkv, Nq, [Nk] * B, d, seed=0, dtype=args.dtype)
+    to = lambda x: to_device(torch, x, dev)
+    table = torch.from_numpy(pin.block_table).to(dev)
+    lens = torch.from_numpy(pin.seqlens).to(dev)
+    q, kc, vc = to(pin.q), to(pin.k_cache), to(pin.v_cache)
+    sets = [(q, kc, vc), (q.clone(), kc.clone(), vc.clone())]
+    o = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    a_bytes = W.bytes_moved(B, Hq, Hkv, Nq, Nk, d) + table.numel() * 4 + lens.numel() * 4
+
+    def step(i):
+        qq, kk, vv = sets[i & 1]
+        fa.fa_decode_paged(qq, kk, vv, table, lens, scale=pin.scale, out=o, lse=lse)
+
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(*device_ids(torch.cuda.get_device_properties(dev)))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = R.slowest_rank_ms(e0.elapsed_time(e1), world, dev)
+    ms = total_ms / args.steps
+    value = R.whole_job_rate(a_bytes / 1e9, args.steps, total_ms, world)
+    if fa.fa_device_status() != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait during the benchmark")
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for f0, f1 in evs:
+        flush.zero_()
+        f0.record(stream)
+        step(0)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    fms = R.slowest_rank_ms(sum(f0.elapsed_time(f1) for f0, f1 in evs), world, dev) / args.steps
+
+    # the same keys stored contiguously, through fa_forward (the decode kernel's other addressing)
+    a = I.make_workload(DECODE_WORKLOAD, dtype=args.dtype)
+    csets = [tuple(to(x) for x in (a.q, a.k, a.v))]
+    csets.append(tuple(x.clone() for x in csets[0]))
+    del sets[1]
+    for i in range(warmup):
+        fa.fa_forward(*csets[i & 1], scale=a.scale, out=o, lse=lse)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(args.steps):
+        fa.fa_forward(*csets[i & 1], scale=a.scale, out=o, lse=lse)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    c_ms = R.slowest_rank_ms(c0.elapsed_time(c1), world, dev) / args.steps
+    del csets
+
+    # end to end: q, both caches, block table and lengths in from pinned host
+    # memory, O and LSE out, every step (nothing overlapped)
+    hin = [x.cpu().pin_memory() for x in (q, kc, vc, table, lens)]
+    hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse)]
+    din = [torch.empty_like(x) for x in (q, kc, vc, table, lens)]
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for dx, hx in zip(din, hin):
+            dx.copy_(hx, non_blocking=True)
+        fa.fa_decode_paged(*din, scale=pin.scale, out=o, lse=lse)
+        hout[0].copy_(o, non_blocking=True)
+        hout[1].copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = R.slowest_rank_ms(x0.elapsed_time(x1), world, dev) / e2e_steps
+    h2d = sum(x.numel() * x.element_size() for x in hin)
+    d2h = sum(x.numel() * x.element_size() for x in hout)
+
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    cpu = None
+    if args.cpu_budget > 0 and world == 1:
+        import oracle
+        t0 = time.perf_counter()
+        n = 0
+        while n == 0 or (time.perf_counter() - t0 < args.cpu_budget and n < B):
+            oracle.paged_attention_reference(pin.q[n:n + 1], pin.k_cache, pin.v_cache, pin.block_table[n:n + 1],
+                                             pin.seqlens[n:n + 1], scale=pin.scale)
+            n += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": a_bytes * n / B / 1e9 / dt, "unit": "GB/s",
+               "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
+               "sample": f"{n} of {B} sequences ({n * Hq} query rows x {Nk} keys) in {dt:.1f} s, FP64 oracle"}
+    line = {
+        "metric": PAGED_METRIC, "pass": "paged", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD + "_paged", "B": B, "H_q": Hq, "H_kv": Hkv, "N_q": Nq,
+                   "seqlens": Nk, "page_keys": I.PAGE_KEYS, "pages": int(pin.k_cache.shape[0]), "d": d,
+                   "causal": False, "scale": pin.scale,
+                   "l2": "inputs larger than L2: two cache sets of 537 MB used in turn, back to back",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": a_bytes / 1e9 / (ms * 1e-3), "peak": peak, "unit": "GB/s",
+                     "frac": a_bytes / 1e9 / (ms * 1e-3) / peak,
+                     "traffic": profiled_traffic(DECODE_WORKLOAD + "_paged", "fa_decode_kernel"),
+                     "peak_source": f"{peak_src} (copy)", "algorithmic_per_launch": a_bytes,
+                     "kernel": "fa_decode_kernel (paged addressing, in-cluster merge)"},
+        "flushed": {"value": a_bytes / 1e9 / (fms * 1e-3), "unit": "GB/s", "ms_per_step": fms,
+                    "note": "each step alone between its own events, L2 flushed before it"},
+        "contiguous": {"value": a_bytes / 1e9 / (c_ms * 1e-3), "unit": "GB/s", "ms_per_step": c_ms,
+                       "note": "the same keys stored contiguously, through fa_forward, same timing"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": a_bytes / 1e9 / (e2e_ms * 1e-3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "note": "fa_decode_paged with torch copies of every input in and O, LSE out, nothing overlapped"},
+        "gpu_launches": fa.fa_forward_plan(B, Hq, Hkv, Nq, Nk, d, False)["launches"] * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,8 +701,9 @@ def main():
                     help="timed steps of the decode workload reported beside the prefill line")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of host time for the cpu_baseline leg (0 disables it)")
-    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
-                    help="backward: time fa_backward on the workload instead (fused impl only)")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "paged"],
+                    help="backward: time fa_backward on the workload instead; paged: the decode "
+                         "workload through fa_decode_paged (fused impl only)")
     args = ap.parse_args()
     if args.impl == "naive" and args.dtype != "bf16":
         ap.error("the unfused baseline is BF16 only")
@@ -554,6 +714,11 @@ def main():
         if args.impl != "fused":
             ap.error("--pass backward times the fused library path only")
         run_backward(args, rank, world, local, warmup)
+        return
+    if args.which == "paged":
+        if args.impl != "fused":
+            ap.error("--pass paged times the fused library path only")
+        run_paged(args, rank, world, local, warmup)
         return
     cfg, a_flops, a_bytes, decode_cfg = workload_config(args.workload)
     unit = "GB/s" if decode_cfg else "TFLOP/s"
