@@ -79,7 +79,8 @@ def forward_loss(q, k, v, do, causal: bool = False, scale: float | None = None) 
     return float((to_f64(do) * o).sum())
 
 
-def backward_error_terms(q, k, v, do, causal: bool = False, scale: float | None = None):
+def backward_error_terms(q, k, v, do, causal: bool = False, scale: float | None = None,
+                         parts: bool = False):
     """Magnitudes that bound what rounding the method's own precision does to
     each gradient (for the tolerance of a 16-bit backward; FP64, same shapes as
     attention_backward's results):
@@ -88,16 +89,18 @@ def backward_error_terms(q, k, v, do, causal: bool = False, scale: float | None 
       (dS is rounded before the dS K product; O enters D rounded to 16 bits);
     * dK: scale |dS|^T |Q|  +  scale P^T (Dabs * |Q|);
     * dV: P^T |dO| (P is rounded before the P^T dO product).
-    A gradient computed with unit roundoff u is within about u (terms + |gradient|)."""
+    A gradient computed with unit roundoff u is within about u (terms + |gradient|).
+    With ``parts`` the terms come back one by one, as a dict: ``dq_ds``, ``dq_d``,
+    ``dk_ds``, ``dk_d``, ``dv_p`` (the first-order effect of rounding dS, D's O,
+    and P respectively)."""
     q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
     B, H_q, n_q, d = q.shape
     H_kv, n_k = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     g = H_q // H_kv
-    tq = np.zeros_like(q)
-    tk = np.zeros_like(k)
-    tv = np.zeros_like(v)
+    out = {"dq_ds": np.zeros_like(q), "dq_d": np.zeros_like(q), "dk_ds": np.zeros_like(k),
+           "dk_d": np.zeros_like(k), "dv_p": np.zeros_like(v)}
     for b in range(B):
         for h in range(H_q):
             hk = h // g
@@ -107,7 +110,11 @@ def backward_error_terms(q, k, v, do, causal: bool = False, scale: float | None 
             dp = doh @ vh.T
             ds = p * (dp - (doh * o).sum(axis=1, keepdims=True))
             dabs = np.abs(doh * o).sum(axis=1, keepdims=True)
-            tq[b, h] = scale * (np.abs(ds) @ np.abs(kh) + dabs * (p @ np.abs(kh)))
-            tk[b, hk] += scale * (np.abs(ds).T @ np.abs(qh) + p.T @ (dabs * np.abs(qh)))
-            tv[b, hk] += p.T @ np.abs(doh)
-    return tq, tk, tv
+            out["dq_ds"][b, h] = scale * (np.abs(ds) @ np.abs(kh))
+            out["dq_d"][b, h] = scale * (dabs * (p @ np.abs(kh)))
+            out["dk_ds"][b, hk] += scale * (np.abs(ds).T @ np.abs(qh))
+            out["dk_d"][b, hk] += scale * (p.T @ (dabs * np.abs(qh)))
+            out["dv_p"][b, hk] += p.T @ np.abs(doh)
+    if parts:
+        return out
+    return out["dq_ds"] + out["dq_d"], out["dk_ds"] + out["dk_d"], out["dv_p"]

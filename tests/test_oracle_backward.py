@@ -87,3 +87,69 @@ def test_bits_inputs_widen_exactly():
     g_f64 = oracle.attention_backward(w(a.q), w(a.k), w(a.v), w(do), causal=True, scale=a.scale)
     for x, y in zip(g_bits, g_f64):
         assert np.array_equal(x, y)
+
+
+# ---- the backward tolerance (backward_error_terms), pinned by simulating on
+# the CPU each rounding a 16-bit backward does, one at a time: P rounded before
+# dV = P^T dO, dS rounded before dQ = scale dS K and dK = scale dS^T Q, and O
+# rounded before D = rowsum(dO * O). Each effect must lie within u times its own
+# term (sound), and reach at least 5 % of it somewhere (not vacuously loose).
+
+def _round_bf16(x):
+    return I.bf16_bits_to_f32(I.f64_to_bf16_bits(x)).astype(np.float64)
+
+
+def _simulated_gradients(a, do, rounded):
+    """dQ, dK, dV in FP64 with one intermediate ("P", "dS" or "O") rounded to BF16."""
+    from oracle.backward import _probabilities
+    q, k, v, g = (oracle.to_f64(x) for x in (a.q, a.k, a.v, do))
+    G = a.H_q // a.H_kv
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(a.B):
+        for h in range(a.H_q):
+            hk = h // G
+            p = _probabilities(q[b, h], k[b, hk], a.N_q, a.N_k, a.causal, a.scale)
+            o = p @ v[b, hk]
+            dv[b, hk] += (_round_bf16(p) if rounded == "P" else p).T @ g[b, h]
+            dd = (g[b, h] * (_round_bf16(o) if rounded == "O" else o)).sum(axis=1, keepdims=True)
+            ds = p * (g[b, h] @ v[b, hk].T - dd)
+            if rounded == "dS":
+                ds = _round_bf16(ds)
+            dq[b, h] = a.scale * ds @ k[b, hk]
+            dk[b, hk] += a.scale * ds.T @ q[b, h]
+    return dq, dk, dv
+
+
+BOUND_SHAPES = [(1, 2, 1, 24, 40, 8, True), (1, 1, 1, 32, 32, 16, False), (2, 2, 2, 20, 12, 8, True)]
+
+
+@pytest.mark.parametrize("shape", BOUND_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_error_terms_cover_each_rounding(shape):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=3)
+    do = I.grad_output(a, seed=3)
+    u = 2.0 ** -8
+    ref = oracle.attention_backward(a.q, a.k, a.v, do, causal=causal, scale=a.scale)
+    t = oracle.backward_error_terms(a.q, a.k, a.v, do, causal=causal, scale=a.scale, parts=True)
+    checks = {"P": [(2, "dv_p")], "dS": [(0, "dq_ds"), (1, "dk_ds")], "O": [(0, "dq_d"), (1, "dk_d")]}
+    for rounded, pairs in checks.items():
+        sim = _simulated_gradients(a, do, rounded)
+        for i, part in pairs:
+            err = np.abs(sim[i] - ref[i])
+            bound = u * t[part]
+            ratio = err / np.where(bound > 0, bound, 1.0)
+            assert np.all(err[bound == 0] < 1e-15), (rounded, part)
+            assert ratio.max() <= 1.0, (rounded, part, ratio.max())
+            assert ratio.max() >= 0.05, (rounded, part, ratio.max())
+        # the gradients this rounding does not touch stay exact
+        for i in set(range(3)) - {i for i, _ in pairs}:
+            assert np.allclose(sim[i], ref[i], rtol=0, atol=1e-12)
+
+
+def test_error_terms_sum_of_parts():
+    a = I.make_inputs(1, 2, 1, 9, 13, 4, causal=True, seed=4)
+    do = I.grad_output(a, seed=4)
+    tq, tk, tv = oracle.backward_error_terms(a.q, a.k, a.v, do, causal=True, scale=a.scale)
+    t = oracle.backward_error_terms(a.q, a.k, a.v, do, causal=True, scale=a.scale, parts=True)
+    assert np.array_equal(tq, t["dq_ds"] + t["dq_d"]) and np.array_equal(tk, t["dk_ds"] + t["dk_d"])
+    assert np.array_equal(tv, t["dv_p"])
