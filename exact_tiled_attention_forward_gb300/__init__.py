@@ -248,6 +248,21 @@ def fa_forward_host_packed(qkvs, outs, shape, causal: bool = False, scale: float
     _check(st, "fa_forward_host_packed")
 
 
+def _check_layout(what, **tensors):
+    """Each named tensor (name -> (tensor, expected shape)) is a contiguous CUDA
+    tensor of that shape: libfa derives every size from the shapes of q and k."""
+    given = [(name, t, shape) for name, (t, shape) in tensors.items() if t is not None]
+    for name, t, shape in given:
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{what}: {name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    for name, t, _ in given:
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: {name} must be contiguous")
+    for name, t, _ in given:
+        if t.numel() > 0 and t.device.type != "cuda":
+            raise ValueError(f"{what}: {name} must be a CUDA tensor")
+
+
 def fa_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None,
                 dk=None, dv=None, stream=None):
     """Gradients (dq, dk, dv) of the forward given its o and lse and the upstream
@@ -262,6 +277,9 @@ def fa_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None =
     if lse is None or lse.dtype != torch.float32:
         raise TypeError("lse (FP32, from the forward) is required")
     B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    qs, ks = (B, H_q, N_q, d), (B, H_kv, N_k, d)
+    _check_layout("fa_backward", q=(q, qs), k=(k, ks), v=(v, ks), o=(o, qs), lse=(lse, (B, H_q, N_q)),
+                  do=(do, qs), dq=(dq, qs), dk=(dk, ks), dv=(dv, ks))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
@@ -295,6 +313,9 @@ def fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, causal: bool = 
         raise ValueError("k_cache / v_cache must be [num_pages, H_kv, 128, d] with q's d")
     if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seqlens_k.shape) != (B,):
         raise ValueError("block_table must be [B, max_pages] and seqlens_k [B]")
+    _check_layout("fa_decode_paged", q=(q, q.shape), k_cache=(k_cache, k_cache.shape),
+                  v_cache=(v_cache, k_cache.shape), block_table=(block_table, block_table.shape),
+                  seqlens_k=(seqlens_k, (B,)), out=(out, q.shape), lse=(lse, (B, H_q, N_q)))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:

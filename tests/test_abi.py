@@ -260,3 +260,38 @@ def test_decode_paged_rejects(lib):
     assert call(pages=1 << 29, Hkv=8, Hq=8) == fa.FA_ERR_INVALID_ARG   # page x head index past 31 bits
     assert call(B=0) == fa.FA_OK                                # nothing to do
 
+
+
+def test_backward_binding_checks_layout(lib):
+    torch = pytest.importorskip("torch")
+    # the binding refuses tensors whose shape, layout or device would let libfa
+    # read past a buffer (all raised before any call into libfa)
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8)
+    with pytest.raises(ValueError, match="do has shape"):
+        fa.fa_backward(q, k, k, q, lse, torch.zeros(1, 2, 7, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="lse has shape"):
+        fa.fa_backward(q, k, k, q, torch.zeros(1, 2, 9), q)
+    with pytest.raises(ValueError, match="contiguous"):
+        fa.fa_backward(q, k, k, q, lse, q.transpose(2, 3).contiguous().transpose(2, 3))
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_backward(q, k, k, q, lse, q)
+    with pytest.raises(TypeError):
+        fa.fa_backward(q, k, k, q, lse.double(), q)
+
+
+def test_decode_paged_binding_checks_layout(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(2, 4, 1, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(3, 2, 128, 64, dtype=torch.bfloat16)
+    table = torch.zeros(2, 2, dtype=torch.int32)
+    lens = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        fa.fa_decode_paged(q, kc, kc, table.long(), lens)
+    with pytest.raises(ValueError, match="128"):
+        fa.fa_decode_paged(q, kc[:, :, :64], kc[:, :, :64], table, lens)
+    with pytest.raises(ValueError, match="block_table"):
+        fa.fa_decode_paged(q, kc, kc, table[:1], lens)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_decode_paged(q, kc, kc, table, lens)
