@@ -16,7 +16,7 @@ Sources (by page and section):
   exp(m_old - m_new) when the max rises; the final output is divided by the
   final sum.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent (the plainest reading each time):
 
 * LSE (the per-row statistic kept for the backward pass, page 3 Step 4) is
   the natural-log log-sum-exp of the *scaled* scores: ``m + ln(l)``.
