@@ -153,3 +153,47 @@ def test_error_terms_sum_of_parts():
     t = oracle.backward_error_terms(a.q, a.k, a.v, do, causal=True, scale=a.scale, parts=True)
     assert np.array_equal(tq, t["dq_ds"] + t["dq_d"]) and np.array_equal(tk, t["dk_ds"] + t["dk_d"])
     assert np.array_equal(tv, t["dv_p"])
+
+
+# ---- closed forms of the definition's gradients
+
+def test_single_key_closed_form():
+    # one key: P = 1 for every row, so O = V_0 whatever Q and K are: dQ = dK = 0
+    # and dV_0 sums dO over every row of every query head that reads it
+    rng = np.random.default_rng(21)
+    q, k, v = rng.normal(size=(2, 4, 5, 3)), rng.normal(size=(2, 2, 1, 3)), rng.normal(size=(2, 2, 1, 3))
+    do = rng.normal(size=(2, 4, 5, 3))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale=0.9)
+    assert np.allclose(dq, 0, atol=1e-14) and np.allclose(dk, 0, atol=1e-14)
+    want = do.reshape(2, 2, 2, 5, 3).sum(axis=(2, 3))[:, :, None, :]
+    assert np.allclose(dv, want, rtol=0, atol=1e-12)
+
+
+def test_zero_queries_closed_form():
+    # Q = 0: every row attends uniformly, P = 1/N_k, so dV_j = (1/N_k) sum_i dO_i
+    # for every key j; dK = scale dS^T Q = 0
+    rng = np.random.default_rng(22)
+    n_q, n_k, d = 6, 7, 4
+    q = np.zeros((1, 1, n_q, d))
+    k, v, do = rng.normal(size=(1, 1, n_k, d)), rng.normal(size=(1, 1, n_k, d)), rng.normal(size=(1, 1, n_q, d))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale=0.5)
+    assert np.allclose(dk, 0, atol=1e-14)
+    assert np.allclose(dv[0, 0], np.tile(do[0, 0].sum(axis=0) / n_k, (n_k, 1)), rtol=0, atol=1e-12)
+    # dQ_i = scale sum_j P_ij (dP_ij - D_i) k_j with P uniform and D_i = dO_i . mean(V)
+    vbar = v[0, 0].mean(axis=0)
+    dp = do[0, 0] @ v[0, 0].T
+    want = 0.5 / n_k * ((dp - (do[0, 0] @ vbar)[:, None]) @ k[0, 0])
+    assert np.allclose(dq[0, 0], want, rtol=0, atol=1e-12)
+
+
+def test_rows_that_see_no_key_contribute_nothing():
+    # causal with N_q > N_k: the first N_q - N_k rows see no key; their dQ is 0 and
+    # removing them (with their dO) leaves dK and dV unchanged
+    rng = np.random.default_rng(23)
+    q, k, v = rng.normal(size=(1, 2, 7, 4)), rng.normal(size=(1, 1, 4, 4)), rng.normal(size=(1, 1, 4, 4))
+    do = rng.normal(size=(1, 2, 7, 4))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True, scale=0.6)
+    assert np.all(dq[:, :, :3] == 0)
+    dq2, dk2, dv2 = oracle.attention_backward(q[:, :, 3:], k, v, do[:, :, 3:], causal=True, scale=0.6)
+    assert np.allclose(dk, dk2, rtol=0, atol=1e-12) and np.allclose(dv, dv2, rtol=0, atol=1e-12)
+    assert np.allclose(dq[:, :, 3:], dq2, rtol=0, atol=1e-12)
