@@ -5,7 +5,10 @@
  * exp(m_old - m_new) when the max rises; O is divided by l once at the end),
  * so the N_q x N_k score and probability matrices never reach device memory.
  * Also returned: the FP32 log-sum-exp of each row's scaled scores, the small
- * per-row statistic the backward pass recomputes from.
+ * per-row statistic the backward pass recomputes from. Around the forward:
+ * its backward pass (fa_backward), decode over a paged K/V cache
+ * (fa_decode_paged), FP16 tensors, host-memory requests, an allocation-free
+ * variant and the unfused baseline.
  *
  * Sources: "Why is standard attention memory-bound, and how does FlashAttention
  * fix it?" (interview.clozo.ai), Step 1 (definition), Step 3 (online softmax),
