@@ -82,6 +82,38 @@ def f64_to_f16(x: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64).astype(np.float16)
 
 
+E4M3_MAX = 448.0   # largest finite FP8 E4M3 value (1.75 * 2^8)
+
+
+def f64_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """float64 -> FP8 E4M3 codes (uint8): 1 sign bit, 4 exponent bits with bias
+    7, 3 mantissa bits, subnormals below 2^-6, no infinities (S.1111.111 is NaN).
+    Round to nearest, ties to even, saturating to +-448 (as a "satfinite"
+    conversion does); NaN maps to 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    a = np.minimum(np.abs(np.nan_to_num(x, nan=0.0)), E4M3_MAX)
+    _, ex = np.frexp(a)                         # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                  # unbiased exponent; subnormals share 2^-6's
+    q = np.rint(np.ldexp(a, 3 - e))             # significand in eighths, ties to even
+    carry = q >= 16                             # rounded up to the next binade
+    e = np.where(carry, e + 1, e)
+    q = np.where(carry, 8, q)
+    normal = q >= 8
+    code = np.where(normal, ((e + 7) << 3) + (q - 8), q).astype(np.uint8)
+    code = code | sign
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def e4m3_power_of_two_scale(x: np.ndarray) -> float:
+    """The smallest power of two s with max|x| / s <= 448 (a per-tensor scale
+    that keeps every value in range; 1.0 for an all-zero tensor)."""
+    amax = float(np.max(np.abs(x))) if np.size(x) else 0.0
+    if amax == 0.0:
+        return 1.0
+    return float(2.0 ** math.ceil(math.log2(amax / E4M3_MAX)))
+
+
 def normal_f16(seed: int, stream: int, shape) -> np.ndarray:
     """The deviates of ``normal_bf16``'s stream, rounded to binary16 instead."""
     count = int(np.prod(shape))
@@ -149,6 +181,9 @@ class AttentionInputs:
     causal: bool
     scale: float
     dtype: str = "bf16"
+    # FP8 ("e4m3") inputs only: per-tensor factors (q, k, v) that turn a decoded
+    # code back into the value it stands for (x = decode(code) * descale)
+    descale: tuple | None = None
 
     @property
     def shape_args(self):
@@ -159,9 +194,14 @@ def make_inputs(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int, *,
                 causal: bool = False, scale: float | None = None, seed: int = 0,
                 k_row_frac: float = 0.0, k_row_factor: float = 8.0,
                 dtype: str = "bf16") -> AttentionInputs:
-    """Draw Q, K, V for one configuration (all ~ N(0, 1); dtype "bf16" or "f16")."""
+    """Draw Q, K, V for one configuration (all ~ N(0, 1); dtype "bf16", "f16",
+    or "e4m3": FP8 codes of x / s with s = ``e4m3_power_of_two_scale`` per
+    tensor, the deviates taken in FP64 from the same streams)."""
+    if dtype == "e4m3":
+        return _make_inputs_e4m3(B, H_q, H_kv, N_q, N_k, d, causal=causal, scale=scale, seed=seed,
+                                 k_row_frac=k_row_frac, k_row_factor=k_row_factor)
     if dtype not in ("bf16", "f16"):
-        raise ValueError(f"dtype must be 'bf16' or 'f16', not {dtype!r}")
+        raise ValueError(f"dtype must be 'bf16', 'f16' or 'e4m3', not {dtype!r}")
     draw = normal_f16 if dtype == "f16" else normal_bf16
     q = draw(seed, STREAM_Q, (B, H_q, N_q, d))
     k = draw(seed, STREAM_K, (B, H_kv, N_k, d))
@@ -178,6 +218,35 @@ def make_inputs(B: int, H_q: int, H_kv: int, N_q: int, N_k: int, d: int, *,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     return AttentionInputs(q, k, v, B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale), dtype)
+
+
+def _normal_array(seed: int, stream: int, shape) -> np.ndarray:
+    count = int(np.prod(shape))
+    out = np.empty(count, dtype=np.float64)
+    for lo in range(0, count, 2 * _CHUNK):
+        hi = min(count, lo + 2 * _CHUNK)
+        out[lo:hi] = _normal_slice(seed, stream, lo, hi)
+    return out.reshape(shape)
+
+
+def _make_inputs_e4m3(B, H_q, H_kv, N_q, N_k, d, *, causal, scale, seed, k_row_frac, k_row_factor):
+    q = _normal_array(seed, STREAM_Q, (B, H_q, N_q, d))
+    k = _normal_array(seed, STREAM_K, (B, H_kv, N_k, d))
+    v = _normal_array(seed, STREAM_V, (B, H_kv, N_k, d))
+    if k_row_frac > 0.0:
+        rows = scaled_rows(seed, B * H_kv, N_k, k_row_frac)
+        kf = k.reshape(B * H_kv, N_k, d)
+        for bh in range(B * H_kv):
+            kf[bh, rows[bh]] *= k_row_factor
+    codes, descale = [], []
+    for x in (q, k, v):
+        s = e4m3_power_of_two_scale(x)
+        codes.append(f64_to_e4m3(x / s))
+        descale.append(s)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return AttentionInputs(codes[0], codes[1], codes[2], B, H_q, H_kv, N_q, N_k, d, bool(causal), float(scale),
+                           "e4m3", tuple(descale))
 
 
 def grad_output(a: AttentionInputs, seed: int = 0) -> np.ndarray:
