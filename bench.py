@@ -502,7 +502,7 @@ def run_backward(args, rank, world, local, warmup):
         cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)),
                "kind": "oracle", "sample": f"{sample}, {dt:.1f} s"}
     line = {
-        "metric": BWD_METRIC, "pass": "backward", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": BWD_METRIC, "pass": "backward", "impl": "fused", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": args.workload, **{k2: cfg[k2] for k2 in
@@ -659,7 +659,7 @@ def run_paged(args, rank, world, local, warmup):
                "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", 1)), "kind": "oracle",
                "sample": f"{n} of {B} sequences ({n * Hq} query rows x {Nk} keys) in {dt:.1f} s, FP64 oracle"}
     line = {
-        "metric": PAGED_METRIC, "pass": "paged", "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": PAGED_METRIC, "pass": "paged", "impl": "fused", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": DECODE_WORKLOAD + "_paged", "B": B, "H_q": Hq, "H_kv": Hkv, "N_q": Nq,
