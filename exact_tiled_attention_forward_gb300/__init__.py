@@ -22,7 +22,9 @@ import re
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libfa.so")
+LIB_SINGLE_GPU_PATH = os.path.join(_PKG, "_build", "libfa_single_gpu.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+HEADER_SINGLE_GPU = os.path.join(os.path.dirname(_PKG), "include", "fa_single_gpu.h")
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -36,6 +38,7 @@ FA_DTYPE_BF16 = 0
 FA_DTYPE_FP16 = 1
 
 _lib = None
+_lib_single = None
 
 
 class FaError(RuntimeError):
@@ -88,9 +91,28 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def header_functions() -> list[str]:
-    """Names of the functions ``include/fa.h`` declares."""
-    text = open(HEADER).read()
+def lib_single_gpu() -> ctypes.CDLL:
+    """Load libfa_single_gpu.so (once): libfa plus the cluster-multicast forward
+    of ``include/fa_single_gpu.h``. Only for a process that uses one GPU."""
+    global _lib_single
+    if _lib_single is None:
+        if not os.path.exists(LIB_SINGLE_GPU_PATH):
+            raise ImportError(f"libfa_single_gpu.so not found at {LIB_SINGLE_GPU_PATH}: build it first "
+                              "(python -m exact_tiled_attention_forward_gb300.build)")
+        l = ctypes.CDLL(LIB_SINGLE_GPU_PATH)
+        sigs = dict(_SIGNATURES)
+        sigs["fa_forward_cluster_multicast"] = _SIGNATURES["fa_forward"]
+        for name, (res, args) in sigs.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib_single = l
+    return _lib_single
+
+
+def header_functions(header: str = HEADER) -> list[str]:
+    """Names of the functions a header (default ``include/fa.h``) declares."""
+    text = open(header).read()
     return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
 
 
@@ -347,6 +369,28 @@ def fa_forward_noalloc(q, k, v, causal: bool = False, scale: float | None = None
     st = lib().fa_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv,
                                   N_q, N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "fa_forward_noalloc")
+    return out, lse
+
+
+def fa_forward_cluster_multicast(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                                 lse=None, return_lse: bool = True, stream=None):
+    """``fa_forward`` (BF16) with CTA pairs sharing K/V tile loads by cluster
+    multicast, from libfa_single_gpu.so (``include/fa_single_gpu.h``): for a
+    process that uses one GPU only. Returns ``(o, lse)``."""
+    import torch
+    _check_dtypes(torch.bfloat16, q, k, v, out, lse)
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    l = lib_single_gpu()
+    st = l.fa_forward_cluster_multicast(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv,
+                                        N_q, N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_forward_cluster_multicast")
     return out, lse
 
 

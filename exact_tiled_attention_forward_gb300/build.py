@@ -1,9 +1,12 @@
-"""Build ``libfa.so`` (the CUDA library behind the C ABI in ``include/fa.h``).
+"""Build ``libfa.so`` (the CUDA library behind the C ABI in ``include/fa.h``)
+and ``libfa_single_gpu.so`` (the same objects plus the cluster-multicast
+forward of ``include/fa_single_gpu.h``, for processes that use one GPU).
 
-Each ``csrc/*.cu`` file is compiled for sm_103a in its own ``nvcc`` process (in
-parallel), then linked into one shared library with the CUDA runtime linked
-statically, so the library depends on nothing but the driver. The result goes
-to ``_build/libfa.so`` inside this package directory.
+Each ``.cu`` file is compiled for sm_103a in its own ``nvcc`` process (in
+parallel), then linked into shared libraries with the CUDA runtime linked
+statically, so they depend on nothing but the driver. ``libfa.so`` is linked
+from ``csrc/`` alone, so it holds no multicast code. The results go to
+``_build/`` inside this package directory.
 """
 from __future__ import annotations
 
@@ -16,9 +19,11 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
+CSRC_SINGLE = os.path.join(PKG, "csrc_single_gpu")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
+LIB_SINGLE_GPU = os.path.join(BUILD, "libfa_single_gpu.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -31,21 +36,22 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfa")
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(folder=CSRC):
+    return sorted(os.path.join(folder, f) for f in os.listdir(folder) if f.endswith(".cu"))
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(LIB_SINGLE_GPU)):
         return True
-    t = os.path.getmtime(LIB)
-    deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    deps.append(os.path.join(INCLUDE, "fa.h"))
+    t = min(os.path.getmtime(LIB), os.path.getmtime(LIB_SINGLE_GPU))
+    deps = sources() + sources(CSRC_SINGLE)
+    for folder in (CSRC, CSRC_SINGLE, INCLUDE):
+        deps += [os.path.join(folder, f) for f in os.listdir(folder) if f.endswith((".cuh", ".h"))]
     return any(os.path.getmtime(f) > t for f in deps)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libfa.so if any source is newer than it; return its path."""
+    """Compile and link both libraries if any source is newer than them; return libfa.so's path."""
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
@@ -61,14 +67,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
+    base, single = sources(), sources(CSRC_SINGLE)
     with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
-        objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        objs = list(ex.map(compile_one, base + single))
+    base_objs, single_objs = objs[:len(base)], objs[len(base):]
+    for out, parts in ((LIB, base_objs), (LIB_SINGLE_GPU, base_objs + single_objs)):
+        tmp = out + ".tmp"
+        cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *parts]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link of {os.path.basename(out)} failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
     return LIB
 
 

@@ -69,7 +69,7 @@ int validate_shape(const Shape& s) {
 }
 
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const Shape& s, float scale) {
+             const Shape& s, float scale, bool check_device) {
   int st = validate_shape(s);
   if (st != FA_OK) return st;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -87,6 +87,30 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (lse && (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
               overlaps(lse, lb, o, qb)))
     return FA_ERR_INVALID_ARG;
+  if (!check_device) return FA_OK;
+  const void* ptrs[5] = {q, rows_k > 0 ? k : nullptr, rows_k > 0 ? v : nullptr, o, lse};
+  return check_current_device(ptrs, 5);
+}
+
+// The kernels and their tensor maps address only the current device's own
+// memory: a host pointer, or memory of another GPU reached through unified
+// addressing, is rejected before anything is enqueued.
+int check_current_device(const void* const* ptrs, int n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int i = 0; i < n; ++i) {
+    if (!ptrs[i]) continue;
+    cudaPointerAttributes a{};
+    e = cudaPointerGetAttributes(&a, ptrs[i]);
+    if (e == cudaErrorInvalidValue) {   // not a pointer the runtime knows
+      cudaGetLastError();
+      return FA_ERR_INVALID_ARG;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != dev)
+      return FA_ERR_INVALID_ARG;
+  }
   return FA_OK;
 }
 
@@ -135,14 +159,6 @@ cudaMemPool_t workspace_pool() {
 }
 
 }  // namespace
-
-// Cluster K/V multicast variant of the fused kernel: FA_MULTICAST=1 turns it on
-// for plans without split tails, 0 (default) keeps the plain kernel. Read at
-// every call, so a process can compare both.
-bool multicast_enabled() {
-  const char* e = getenv("FA_MULTICAST");
-  return e && e[0] == '1';
-}
 
 // In-cluster merge of split partials: on unless FA_CLUSTER_MERGE=0 (read at every call).
 bool cluster_merge_enabled() {
@@ -327,7 +343,7 @@ FwdPlan prefill_plan(int B, int H_q, int N_q, int N_k, int d, int causal) {
 
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t strm,
-                 const WorkspaceSource& wsrc, int elem) {
+                 const WorkspaceSource& wsrc, int elem, PairedLaunch paired) {
   if (elem != 0 && elem != 1) return FA_ERR_INVALID_ARG;
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
   int st = validate(q, k, v, o, lse, s, scale);
@@ -394,8 +410,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.s_tail = pl.s_tail;
   p.n_units = (int)pl.units;
   p.cm = pl.cluster_merge;
-  // (the multicast variant is built for BF16 only)
-  const bool multicast = pl.n_tail == 0 && pl.units >= 2 && elem == 0 && multicast_enabled();
+  // (the paired-load variant is built for BF16 only)
+  const bool multicast = paired && pl.n_tail == 0 && pl.units >= 2 && elem == 0;
   p.elem = elem;
   p.n_bh = B * H_q;
   // the multicast variant pairs adjacent blocks of one head: head-major there
@@ -427,7 +443,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
       return cuda_fail(cudaErrorInvalidValue);
     }
   }
-  cudaError_t e = launch_fwd(d, maps, p, (int)pl.units, multicast, strm);
+  cudaError_t e = multicast ? paired(d, maps, p, (int)pl.units, strm)
+                            : launch_fwd(d, maps, p, (int)pl.units, strm);
   if (ws && wsrc.release) wsrc.release(ws, strm);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -494,7 +511,6 @@ int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causa
   } else {
     const fa::FwdPlan pl = fa::prefill_plan(B, H_q, N_q, N_k, d, causal);
     c = pl.units;
-    if (pl.n_tail == 0 && pl.units >= 2 && fa::multicast_enabled()) c = (pl.units + 1) & ~1ll;
     n = pl.part_bytes > 0 ? 2 : 1;
     ws = pl.part_bytes;
   }
@@ -526,11 +542,15 @@ int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float
                      int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
                      void* workspace, size_t workspace_bytes, void* stream) {
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
-  int st = validate(q, k, v, o, lse, s, scale);
+  int st = validate(q, k, v, o, lse, s, scale, false);
   if (st != FA_OK) return st;
   if ((long long)B * H_q * N_q == 0) return FA_OK;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  if (N_k == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
+  if (N_k == 0) {
+    const void* outs[2] = {o, lse};
+    st = check_current_device(outs, 2);
+    return st != FA_OK ? st : fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
+  }
   const size_t need = fa_naive_workspace_bytes(B, H_q, N_q, N_k);
   if (!workspace || workspace_bytes < need) return FA_ERR_NO_MEMORY;
   if (!aligned16(workspace)) return FA_ERR_INVALID_ARG;
@@ -539,6 +559,9 @@ int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float
       overlaps(workspace, need, v, kb) || overlaps(workspace, need, o, qb) ||
       overlaps(workspace, need, lse, lse ? (size_t)B * H_q * N_q * 4 : 0))
     return FA_ERR_INVALID_ARG;
+  const void* ptrs[6] = {q, k, v, o, lse, workspace};
+  st = check_current_device(ptrs, 6);
+  if (st != FA_OK) return st;
   int* status = device_status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
 

@@ -707,6 +707,13 @@ int backward_impl(const void* q, const void* k, const void* v, const void* o, co
     for (int j = 0; j < i; ++j)
       if (overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return FA_ERR_INVALID_ARG;
   }
+  {
+    const void* all[9];
+    for (int i = 0; i < 6; ++i) all[i] = in_bytes[i] ? ins[i] : nullptr;
+    for (int i = 0; i < 3; ++i) all[6 + i] = out_bytes[i] ? outs[i] : nullptr;
+    st = check_current_device(all, 9);
+    if (st != FA_OK) return st;
+  }
   // nothing to differentiate through: every gradient that exists is zero
   if (rows_q == 0 || rows_k == 0) {
     for (int i = 0; i < 3; ++i) {

@@ -53,17 +53,19 @@ int fwd_cluster_capacity(int d, int s);
 // Shared-memory bytes the fused kernel needs for head dim d (64 or 128).
 size_t fwd_smem_bytes(int d);
 
-// Launch the fused kernel over `units` CTAs, then (if p.n_tail > 0) the merge
-// kernel as its programmatic dependent on the same stream. With multicast,
-// CTAs run in clusters of two that share K/V tile loads (no split plans;
-// tk / tv must then be built with 64-row boxes).
 // Tensor maps of one forward call: Q, K, V, O (BF16, [B*H][N][d], 64-column
 // boxes, 128-byte swizzle) and the FP32 split partials ([rows][d], 32-column boxes).
 struct FwdMaps {
   CUtensorMap q, k, v, o, part;
 };
-cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, bool multicast,
-                       cudaStream_t stream);
+// Launch the fused kernel over `units` CTAs, then (if p.n_tail > 0) the merge
+// kernel as its programmatic dependent on the same stream.
+cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, cudaStream_t stream);
+// A launcher of the paired-load variant (CTAs in clusters of two sharing K/V
+// tile loads by cluster multicast; plans without split tails; tk / tv built
+// with 64-row boxes). Only the single-GPU library has one; libfa passes none.
+typedef cudaError_t (*PairedLaunch)(int d, const FwdMaps& m, const FwdParams& p, int units,
+                                    cudaStream_t stream);
 
 // ---- decode / few queries per KV head -------------------------------------------------
 constexpr int kDecodeMaxRows = 16;   // R = G * N_q rows per KV head must fit one m16 MMA
@@ -132,9 +134,10 @@ struct Shape {
 };
 // Shape checks alone (sizes, H_q % H_kv, 32-bit row counts, d): fa_status code.
 int validate_shape(const Shape& s);
-// Argument checks shared by the forward entry points (fa_status code; FA_OK when valid).
+// Argument checks shared by the forward entry points (fa_status code; FA_OK when valid);
+// check_device: also require every pointer to be memory of the current device.
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const Shape& s, float scale);
+             const Shape& s, float scale, bool check_device = true);
 // O = 0 and LSE = -inf for `rows` rows (every row sees no key).
 int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st);
 // Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA; the
@@ -176,8 +179,13 @@ struct WorkspaceSource {
 const WorkspaceSource& pool_workspace();   // library-owned stream-ordered pool
 // The whole fused forward (validation, decode or prefill plan, launches);
 // elem: 0 = BF16, 1 = FP16 tensors.
+// paired: the paired-load launcher, used for BF16 plans without split tails
+// (nullptr: the plain kernel always).
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t stream,
-                 const WorkspaceSource& ws, int elem = 0);
+                 const WorkspaceSource& ws, int elem = 0, PairedLaunch paired = nullptr);
+// Every non-null pointer is device memory of the current device (FA_OK),
+// else FA_ERR_INVALID_ARG; FA_ERR_CUDA when the device cannot be queried.
+int check_current_device(const void* const* ptrs, int n);
 
 }  // namespace fa

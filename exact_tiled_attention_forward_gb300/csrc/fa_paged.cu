@@ -56,6 +56,11 @@ int paged_impl(const void* q, const void* k_cache, const void* v_cache, const in
     if (overlap(o, qb, ins[i], in_bytes[i]) || (lse && overlap(lse, lb, ins[i], in_bytes[i])))
       return FA_ERR_INVALID_ARG;
   if (lse && overlap(lse, lb, o, qb)) return FA_ERR_INVALID_ARG;
+  {
+    const void* all[7] = {q, k_cache, v_cache, block_table, seqlens, o, lse};
+    const int dst = check_current_device(all, 7);
+    if (dst != FA_OK) return dst;
+  }
 
   int* status = device_status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());

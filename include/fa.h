@@ -20,8 +20,13 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - All tensor pointers are DEVICE pointers owned by the caller; the library
- *    keeps no reference after the call returns.
+ *  - All tensor pointers are DEVICE pointers of the CURRENT device, owned by
+ *    the caller; the library keeps no reference after the call returns. A
+ *    pointer to host memory (pinned or not) or to another GPU's memory is
+ *    rejected with FA_ERR_INVALID_ARG before anything is enqueued.
+ *  - Per-device state (the status word's address, the scratch array's
+ *    address, the workspace pool) is looked up once per device and kept for
+ *    the life of the process: do not use libfa across cudaDeviceReset.
  *  - q: BF16 [B][H_q][N_q][d];  k, v: BF16 [B][H_kv][N_k][d];  o: BF16
  *    [B][H_q][N_q][d]; lse: FP32 [B][H_q][N_q] or NULL. All contiguous,
  *    row-major, 16-byte aligned.
@@ -92,8 +97,7 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
  * tensors in FP16 ("Flash Attention Mechanics", its opening and "Why Standard
  * Attention Is Memory-Bound"; "Why is standard attention memory-bound...",
  * Step 1). P is rounded to FP16 before the P V product; a row's exponentials are kept
- * at most 2^15 against a reference max, so they never overflow FP16. The paired
- * multicast loads (FA_MULTICAST=1) are BF16-only and are not used here. */
+ * at most 2^15 against a reference max, so they never overflow FP16. */
 int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
                     void* stream);
@@ -225,10 +229,9 @@ size_t fa_naive_workspace_bytes(int B, int H_q, int N_q, int N_k);
  * kernel follows); *workspace_bytes = stream-ordered workspace the call
  * allocates, which is also the scratch fa_forward_noalloc needs (0 when the
  * split partials are merged inside thread-block clusters). The plan depends on
- * the device's SM count and cluster capacity, and on the environment switches
- * FA_CLUSTER_MERGE=0 (merge kernel instead of in-cluster merge) and
- * FA_MULTICAST=1 (paired K/V loads). Returns FA_OK, FA_ERR_INVALID_ARG or
- * FA_ERR_UNSUPPORTED. */
+ * the device's SM count and cluster capacity, and on the environment switch
+ * FA_CLUSTER_MERGE=0 (merge kernel instead of in-cluster merge). Returns FA_OK,
+ * FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED. */
 int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal, long long* ctas,
                     int* launches, size_t* workspace_bytes);
 

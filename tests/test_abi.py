@@ -36,6 +36,41 @@ def test_header_symbols_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_single_gpu_library_exports_both_headers(lib):
+    # libfa_single_gpu.so = libfa's entry points + the cluster-multicast forward;
+    # libfa.so itself has no multicast entry point
+    if not os.path.exists(fa.LIB_SINGLE_GPU_PATH):
+        fa_build.build()
+    single = fa.lib_single_gpu()
+    extra = fa.header_functions(fa.HEADER_SINGLE_GPU)
+    assert extra == ["fa_forward_cluster_multicast"]
+    for n in fa.header_functions() + extra:
+        assert hasattr(single, n), n
+    assert not hasattr(lib, "fa_forward_cluster_multicast")
+
+
+def test_default_library_sources_hold_no_multicast():
+    # the sources libfa.so is linked from never name a cluster-multicast copy or commit
+    for name in os.listdir(fa_build.CSRC):
+        text = open(os.path.join(fa_build.CSRC, name)).read()
+        assert "multicast::cluster" not in text, name
+    assert any("multicast::cluster" in open(os.path.join(fa_build.CSRC_SINGLE, n)).read()
+               for n in os.listdir(fa_build.CSRC_SINGLE))
+
+
+def test_single_gpu_forward_refuses_multi_process_jobs(lib, monkeypatch):
+    # checked before anything else: a rank of a multi-process job gets UNSUPPORTED
+    if not os.path.exists(fa.LIB_SINGLE_GPU_PATH):
+        fa_build.build()
+    f = fa.lib_single_gpu().fa_forward_cluster_multicast
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 128, 0, 0.125, None) == fa.FA_ERR_UNSUPPORTED
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    # otherwise it validates like fa_forward
+    assert f(Q, K, V, O, L, 1, 3, 2, 64, 64, 128, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, 7):
         s = fa.fa_status_string(code)

@@ -264,3 +264,38 @@ def test_naive_one_head_n8192(fa):
     o_ref, lse_ref, a_ref = run_oracle(a)
     compare(o, None, o_ref, None, a_ref, tol_o=2e-2, tol_rel=1e-2)
     assert np.all(np.abs(lse - lse_ref) <= naive_lse_bound(a))
+
+
+def test_rejects_memory_not_on_the_current_device(fa):
+    # every pointer must be memory of the current GPU: pinned host memory (which
+    # the GPU could reach) and ordinary host memory are refused before anything
+    # is enqueued; the same call with device tensors runs
+    import torch
+    a = I.make_inputs(1, 2, 1, 200, 300, 128, causal=True, seed=12)
+    q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
+    o = torch.zeros((1, 2, 200, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 2, 200), dtype=torch.float32, device="cuda")
+    pinned = q.cpu().pin_memory()
+    plain = np.zeros(q.numel() + 64, dtype=np.uint16)
+    addr = plain.ctypes.data
+    host_ptr = addr + (-addr) % 16          # 16-byte aligned host address
+    L = fa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    args = lambda qq, oo: (qq, k.data_ptr(), v.data_ptr(), oo, lse.data_ptr(), 1, 2, 1, 200, 300, 128, 1,
+                           a.scale, stream)
+    for bad_q in (pinned.data_ptr(), host_ptr):
+        assert L.fa_forward(*args(bad_q, o.data_ptr())) == fa.FA_ERR_INVALID_ARG
+        assert L.fa_forward_noalloc(*args(bad_q, o.data_ptr())) == fa.FA_ERR_INVALID_ARG
+    pinned_o = torch.zeros((1, 2, 200, 128), dtype=torch.bfloat16).pin_memory()
+    assert L.fa_forward(*args(q.data_ptr(), pinned_o.data_ptr())) == fa.FA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(pinned_o == 0)
+    assert L.fa_forward(*args(q.data_ptr(), o.data_ptr())) == fa.FA_OK
+    torch.cuda.synchronize()
+    compare(bf16_dev_to_f64(o), lse.cpu().numpy().astype(np.float64), *run_oracle(a))
+    # the backward and the paged decode check their pointers the same way
+    dq = torch.empty_like(q)
+    st = L.fa_backward(pinned.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       o.data_ptr(), dq.data_ptr(), torch.empty_like(k).data_ptr(),
+                       torch.empty_like(v).data_ptr(), 1, 2, 1, 200, 300, 128, 1, a.scale, 0, stream)
+    assert st == fa.FA_ERR_INVALID_ARG

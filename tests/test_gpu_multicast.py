@@ -1,12 +1,11 @@
-"""GPU parity of the thread-block-cluster K/V multicast variant (FA_MULTICAST=1):
+"""GPU parity of the thread-block-cluster K/V multicast variant
+(fa_forward_cluster_multicast, libfa_single_gpu.so, a one-GPU process only):
 clusters of two CTAs of one head fetch each K/V tile once and multicast it into
 both CTAs' shared memory. Same oracle and tolerances as the plain kernel;
 includes pairs that straddle two heads (odd number of query blocks per head),
 an idle CTA completing the last cluster, causal pairs with unequal key ranges,
 GQA and ragged lengths. Results must also equal the plain kernel's bit for bit
 (same arithmetic, only the loads differ)."""
-import os
-
 import numpy as np
 import pytest
 
@@ -31,17 +30,11 @@ def fa():
 
 def _run(fa, a, multicast):
     import torch
-    old = os.environ.get("FA_MULTICAST")
-    os.environ["FA_MULTICAST"] = "1" if multicast else "0"
-    try:
-        o, lse = fa.fa_forward(to_dev(a.q), to_dev(a.k), to_dev(a.v), causal=a.causal, scale=a.scale)
-        torch.cuda.synchronize()
-    finally:
-        if old is None:
-            del os.environ["FA_MULTICAST"]
-        else:
-            os.environ["FA_MULTICAST"] = old
-    assert fa.fa_device_status() == fa.FA_OK
+    fn = fa.fa_forward_cluster_multicast if multicast else fa.fa_forward
+    o, lse = fn(to_dev(a.q), to_dev(a.k), to_dev(a.v), causal=a.causal, scale=a.scale)
+    torch.cuda.synchronize()
+    status = fa.lib_single_gpu().fa_device_status(1) if multicast else fa.fa_device_status()
+    assert status == fa.FA_OK
     return bf16_dev_to_f64(o), lse.cpu().numpy().astype(np.float64)
 
 
