@@ -3,21 +3,45 @@ import numpy as np
 
 import oracle
 
-# Tolerances on BF16 inputs (FP32 accumulate, BF16 output)
+# Tolerances on BF16 inputs (FP32 accumulate, BF16 output), as stated for the
+# method: max|dO| <= 1e-2, relative L2 <= 5e-3, max|dLSE| <= 1e-3.
 TOL_MAX_ABS_O = 1e-2
 TOL_REL_L2_O = 5e-3
 TOL_MAX_ABS_LSE = 1e-3
-# Element-wise, the absolute bound on O is widened where the BF16 arithmetic
-# the method fixes cannot meet 1e-2: BF16 has unit roundoff u = 2^-8, so
-#   * rounding O itself to BF16 moves it by up to u |O|, and
-#   * each probability is rounded to BF16 before the PV product, which moves
-#     O_t = sum_j p_j v_jt / l by up to u * A_t with A_t = sum_j p_j |v_jt| / l.
-# A is the oracle's own definition evaluated on |V|. Each element must satisfy
-#   |dO| <= max(1e-2, TOL_REL_ELEM_O * (A + |O_ref|))   (5e-3 = 1.28 u).
-TOL_REL_ELEM_O = 5e-3
-# The same derivation with FP16's unit roundoff u = 2^-11 (P and O rounded to
-# FP16): 1.28 u = 6.25e-4; the absolute floor (1e-2) stays the stated one.
-TOL_REL_ELEM_O_F16 = 6.25e-4
+# Element-wise, where the 16-bit arithmetic cannot meet 1e-2, the bound on an
+# element of O is what that arithmetic allows (unit roundoff u = 2^-8 in BF16,
+# 2^-11 in FP16):
+#   * every probability is rounded to the element type before the P V product,
+#     which moves O_t = sum_j p_j v_jt / l by at most u * A_t, where
+#     A_t = sum_j p_j |v_jt| / l (the oracle's attention applied to |V|);
+#   * the computed value, whose magnitude is at most |O_ref| + u A, is then
+#     rounded to the element type: at most half the type's spacing there;
+#   * FP32 accumulation over N_k keys and the exponential's approximation add
+#     errors of order sqrt(N_k) * 2^-24 * A, covered by 2^-16 * A (N_k <= 2^16).
+#   |dO| <= max(1e-2, half_spacing(|O_ref| + u A) + (u + 2^-16) A)
+# (1e-2 is the stated bound; the second term exceeds it only where |O_ref| or
+# A is at least about 1.3, e.g. rows whose weight sits on a few scaled keys.)
+U_BF16 = 2.0 ** -8
+U_F16 = 2.0 ** -11
+U_ACC = 2.0 ** -16
+
+
+def half_spacing(x, elem="bf16"):
+    """Half the distance between adjacent values of the 16-bit type at |x|
+    (8 significant bits in BF16, 11 in FP16 with its subnormal floor 2^-24)."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(x)                     # x = m 2^e, 0.5 <= m < 1: x in [2^(e-1), 2^e)
+    if elem == "f16":
+        return np.ldexp(1.0, np.maximum(e, -13) - 12)
+    return np.ldexp(1.0, e - 9)
+
+
+def elementwise_bound(o_ref, a_ref, elem="bf16", floor=TOL_MAX_ABS_O):
+    """Per-element bound on |O_gpu - O_ref| (see the derivation above)."""
+    u = U_F16 if elem == "f16" else U_BF16
+    o_ref = np.abs(np.asarray(o_ref, dtype=np.float64))
+    a_ref = np.asarray(a_ref, dtype=np.float64)
+    return np.maximum(floor, half_spacing(o_ref + u * a_ref, elem) + (u + U_ACC) * a_ref)
 
 
 def abs_values(v):
@@ -44,10 +68,23 @@ def bf16_dev_to_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def _log_parity(res):
+    """Append this comparison's figures to $FA_PARITY_LOG (JSON lines) if set."""
+    import json
+    import os
+    path = os.environ.get("FA_PARITY_LOG")
+    if path:
+        rec = dict(res, test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0])
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
             tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE, elem="bf16"):
-    """Element-wise comparison of O and LSE; returns a dict of error figures.
-    ``elem`` ("bf16" or "f16") picks the element-wise relative bound."""
+    """Element-wise comparison of O and LSE; returns a dict of error figures,
+    including how many elements of O differ by more than the stated 1e-2
+    (``n_over_1e2``) and the largest |O_ref| among them. ``o_abs_ref`` is A (the
+    oracle's attention of |V|); ``elem`` ("bf16" or "f16") the element type."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape
@@ -55,12 +92,14 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
     err = np.abs(o_gpu - o_ref)
     max_abs = float(err.max()) if err.size else 0.0
     a_ref = np.abs(o_ref) if o_abs_ref is None else np.asarray(o_abs_ref, dtype=np.float64)
-    rel_elem = TOL_REL_ELEM_O_F16 if elem == "f16" else TOL_REL_ELEM_O
-    bound = np.maximum(tol_o, rel_elem * (a_ref + np.abs(o_ref)))
+    bound = elementwise_bound(o_ref, a_ref, elem, floor=tol_o)
     worst = float((err / bound).max()) if err.size else 0.0
+    over = err > TOL_MAX_ABS_O
     denom = float(np.linalg.norm(o_ref))
     rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))
-    res = {"max_abs_o": max_abs, "rel_l2_o": rel, "worst_over_bound": worst}
+    res = {"max_abs_o": max_abs, "rel_l2_o": rel, "worst_over_bound": worst,
+           "n_elems": int(err.size), "n_over_1e2": int(over.sum()),
+           "max_abs_oref_over_1e2": float(np.abs(o_ref[over]).max()) if over.any() else 0.0}
     if lse_ref is not None:
         lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
         inf_ref = np.isneginf(lse_ref)
@@ -68,7 +107,9 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
         fin = ~inf_ref
         lerr = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
         res["max_abs_lse"] = lerr
-        assert lerr <= tol_lse, res
+    _log_parity(res)
+    if lse_ref is not None:
+        assert res["max_abs_lse"] <= tol_lse, res
     assert worst <= 1.0, res
     assert rel <= tol_rel, res
     return res

@@ -15,7 +15,7 @@ import pytest
 
 from exact_tiled_attention_forward_gb300 import inputs as I
 
-from helpers import TOL_MAX_ABS_O, TOL_REL_ELEM_O, TOL_REL_L2_O, TOL_MAX_ABS_LSE, to_dev
+from helpers import compare, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,8 @@ def _planned_scratch(fa, a):
     # split partials through the scratch array (merge kernel)
     ((1, 1, 1, 8192, 8192, 128, False), False),   # one head, N = 8192: split over 4 CTAs per block
     ((1, 2, 1, 700, 3000, 64, True), False),      # causal, GQA, ragged, d = 64
+    # decode partials through the scratch array (chunk-merge kernel)
+    ((2, 8, 2, 1, 4096, 128, False), False),      # GQA 4, one query row: runs of 128-key chunks
     # split partials merged inside clusters: no scratch at all
     ((1, 1, 1, 8192, 8192, 128, False), True),
 ])
@@ -69,8 +71,10 @@ def test_noalloc_matches_fa_forward_twice(fa, shape, cluster_merge, monkeypatch)
     o_ref = torch.empty((a.B, a.H_q, a.N_q, a.d), dtype=torch.bfloat16, device="cuda")
     l_ref = torch.empty((a.B, a.H_q, a.N_q), dtype=torch.float32, device="cuda")
     assert _call(fa, "fa_forward", q, k, v, o_ref, l_ref, a) == fa.FA_OK
+    torch.cuda.synchronize()
     ref_o = o_ref.float().cpu().numpy()
     ref_l = l_ref.cpu().numpy()
+    oracle_o, oracle_l, oracle_a = run_oracle(a)
     for _ in range(2):   # two calls in a row: the array keeps the previous call's contents
         o = torch.full_like(o_ref, float("nan"))
         l = torch.full_like(l_ref, float("nan"))
@@ -79,13 +83,11 @@ def test_noalloc_matches_fa_forward_twice(fa, shape, cluster_merge, monkeypatch)
         assert fa.fa_device_status() == fa.FA_OK
         got_o = o.float().cpu().numpy()
         got_l = l.cpu().numpy()
-        assert np.isfinite(got_o).all()
-        err = np.abs(got_o - ref_o)
-        assert (err <= np.maximum(TOL_MAX_ABS_O, TOL_REL_ELEM_O * np.abs(ref_o))).all()
-        assert np.linalg.norm(got_o - ref_o) <= TOL_REL_L2_O * np.linalg.norm(ref_o)
-        fin = np.isfinite(ref_l)
-        assert np.array_equal(np.isfinite(got_l), fin)
-        assert np.abs(got_l[fin] - ref_l[fin]).max() <= TOL_MAX_ABS_LSE
+        # the same kernels and the same split as fa_forward: the same bits
+        assert np.array_equal(got_o, ref_o)
+        assert np.array_equal(got_l, ref_l)
+        # and within the method's tolerances of the FP64 oracle
+        compare(got_o.astype(np.float64), got_l.astype(np.float64), oracle_o, oracle_l, oracle_a)
 
 
 def test_noalloc_rejects_requests_beyond_scratch(fa, monkeypatch):
