@@ -18,7 +18,7 @@ TOL_MAX_ABS_LSE = 1e-3
 #     rounded to the element type: at most half the type's spacing there;
 #   * FP32 accumulation over N_k keys and the exponential's approximation add
 #     errors of order sqrt(N_k) * 2^-24 * A, covered by 2^-16 * A (N_k <= 2^16).
-#   |dO| <= max(1e-2, half_spacing(|O_ref| + u A) + (u + 2^-16) A)
+#   |dO| <= max(1e-2, half_spacing(|O_ref| + u' A) + u' A),  u' = u + 2^-16
 # (1e-2 is the stated bound; the second term exceeds it only where |O_ref| or
 # A is at least about 1.3, e.g. rows whose weight sits on a few scaled keys.)
 U_BF16 = 2.0 ** -8
@@ -38,10 +38,10 @@ def half_spacing(x, elem="bf16"):
 
 def elementwise_bound(o_ref, a_ref, elem="bf16", floor=TOL_MAX_ABS_O):
     """Per-element bound on |O_gpu - O_ref| (see the derivation above)."""
-    u = U_F16 if elem == "f16" else U_BF16
+    u = (U_F16 if elem == "f16" else U_BF16) + U_ACC
     o_ref = np.abs(np.asarray(o_ref, dtype=np.float64))
     a_ref = np.asarray(a_ref, dtype=np.float64)
-    return np.maximum(floor, half_spacing(o_ref + u * a_ref, elem) + (u + U_ACC) * a_ref)
+    return np.maximum(floor, half_spacing(o_ref + u * a_ref, elem) + u * a_ref)
 
 
 def abs_values(v):
