@@ -48,6 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # used only while their hash matches the one recorded with it)
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
+                      "exact_tiled_attention_forward_gb300/csrc/fa_fwd_kernel.cuh",
                       "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
     "fa_decode_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
                          "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
@@ -213,14 +214,22 @@ def device_ids(props):
 
 def to_device(torch, x, dev):
     """An input array on the device: FP16 values as torch.float16, BF16 bit
-    patterns as torch.bfloat16."""
-    if x.dtype == np.float16:
-        return torch.from_numpy(x).to(dev)
+    patterns as torch.bfloat16, FP8 E4M3 codes as torch.uint8."""
+    if x.dtype == np.float16 or x.dtype == np.uint8:
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
     return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
 
 
 def elem_dtype(torch, a):
+    """Element type of O (BF16 for FP8 inputs)."""
     return torch.float16 if a.dtype == "f16" else torch.bfloat16
+
+
+def forward_fn(fa, a):
+    """The library's forward for the workload's input type, as fn(q, k, v, ...)."""
+    if a.dtype == "e4m3":
+        return lambda q, k, v, **kw: fa.fa_forward_fp8(q, k, v, a.descale, **kw)
+    return fa.fa_forward
 
 
 def workload_config(name: str):
@@ -239,6 +248,9 @@ def cpu_oracle_throughput(a, budget_s: float, max_rows: int | None = None):
     Returns (rows done, seconds, threads used, (batch, head) calls)."""
     import oracle
     B, Hq, Hkv, Nq, Nk, d = a.shape_args
+    q, k, v = a.q, a.k, a.v
+    if a.dtype == "e4m3":   # the FP8 oracle: the definition on code * factor
+        q, k, v = (oracle.e4m3_to_f64(x) * s for x, s in zip((q, k, v), a.descale))
     t0 = time.perf_counter()
     done_rows = 0
     calls = 0
@@ -248,8 +260,7 @@ def cpu_oracle_throughput(a, budget_s: float, max_rows: int | None = None):
                 n = Nq if max_rows is None else min(Nq, max_rows - done_rows)
                 if n <= 0:
                     break
-                oracle.attention_rows(a.q, a.k, a.v, b, h, np.arange(n), causal=a.causal,
-                                      scale=a.scale)
+                oracle.attention_rows(q, k, v, b, h, np.arange(n), causal=a.causal, scale=a.scale)
                 done_rows += n
                 calls += 1
                 if time.perf_counter() - t0 >= budget_s and max_rows is None:
@@ -340,7 +351,7 @@ def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_
     o_bytes, l_bytes = B * Hq * Nq * d * 2, B * Hq * Nq * 4
     hout = [torch.empty(o_bytes + l_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
 
-    if ws is None:
+    if ws is None and a.dtype != "e4m3":
         def run(n):
             fa.fa_forward_host_packed([hin] * n, [hout[i & 1] for i in range(n)], a.shape_args,
                                       causal=a.causal, scale=a.scale, dtype=el)
@@ -352,10 +363,12 @@ def time_e2e(torch, fa, a, cfg, dev, stream, fn, ws, steps, warmup, world, work_
         do = dout[:o_bytes].view(el).view(B, Hq, Nq, d)
         dl = dout[o_bytes:].view(torch.float32).view(B, Hq, Nq)
 
+        extra = {} if ws is None else {"workspace": ws}
+
         def run(n):
             for _ in range(n):
                 din.copy_(hin, non_blocking=True)
-                fn(dq, dk, dv, causal=a.causal, scale=a.scale, out=do, lse=dl, workspace=ws)
+                fn(dq, dk, dv, causal=a.causal, scale=a.scale, out=do, lse=dl, **extra)
                 hout[0].copy_(dout, non_blocking=True)
 
     run(max(3, warmup))
@@ -707,8 +720,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fused", choices=["fused", "naive", "reference"])
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
-                    help="element type of Q, K, V and O (the unfused baseline is BF16 only)")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16", "e4m3"],
+                    help="element type of Q, K, V (and O; BF16 O for e4m3 inputs, which run "
+                         "fa_forward_fp8 with per-tensor factors); the unfused baseline is BF16 only")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--decode-steps", type=int, default=500,
                     help="timed steps of the decode workload reported beside the prefill line")
@@ -720,6 +734,10 @@ def main():
     args = ap.parse_args()
     if args.impl == "naive" and args.dtype != "bf16":
         ap.error("the unfused baseline is BF16 only")
+    if args.dtype == "e4m3" and args.which != "forward":
+        ap.error("e4m3 inputs: forward pass only")
+    if args.dtype == "e4m3":
+        args.decode_steps = 0   # the secondary decode line is the BF16 decode workload
     warmup = max(3, args.warmup)
 
     rank, world, local = R.replica_env()
@@ -787,7 +805,7 @@ def main():
         return to_device(torch, x, dev)
 
     q, k, v = to_dev(a.q), to_dev(a.k), to_dev(a.v)
-    fn = fa.fa_forward if args.impl == "fused" else fa.fa_naive_forward
+    fn = forward_fn(fa, a) if args.impl == "fused" else fa.fa_naive_forward
     ws = None
     if args.impl == "naive":
         ws = torch.empty(fa.fa_naive_workspace_bytes(B, Hq, Nq, Nk), dtype=torch.uint8, device=dev)
@@ -796,7 +814,7 @@ def main():
     # Input sets: copies of the same Q, K, V (and their own O, LSE), used in turn,
     # enough of them that the inputs of all sets together take at least twice
     # the L2 size: a step's inputs have left L2 by the time its set comes round again.
-    set_bytes = (q.numel() + k.numel() + v.numel()) * 2
+    set_bytes = (q.numel() + k.numel() + v.numel()) * q.element_size()
     n_sets = min(4096, max(2, -(-2 * l2_bytes // set_bytes)))
     # one copy kernel per input: [n_sets, ...] tensors whose slices are the sets
     qs, ks, vs = (x.unsqueeze(0).expand(n_sets, *x.shape).contiguous() for x in (q, k, v))
@@ -880,14 +898,21 @@ def main():
         achieved = a_bytes / 1e9 / (ms_per_step * 1e-3)
         roof = {"bound": "hbm", "unit": "GB/s"}
     else:
-        peak = float(peaks["bf16_tflops"])
+        # FP8 MMAs: the measured BF16 peak times the nominal FP8 / BF16 ratio (4.5 / 2.25 PF)
+        peak = float(peaks["bf16_tflops"]) * (2.0 if args.dtype == "e4m3" else 1.0)
         achieved = a_flops / 1e12 / (ms_per_step * 1e-3)
         roof = {"bound": "tensor", "unit": "TFLOP/s"}
-    traffic = profiled_traffic(args.workload) if args.impl == "fused" else None
+    traffic = (profiled_traffic(args.workload + ("_e4m3" if args.dtype == "e4m3" else ""))
+               if args.impl == "fused" else None)
+    if args.dtype == "bf16" or decode_cfg:
+        peak_src_note = f"{peak_src} (burst)"
+    elif args.dtype == "e4m3":
+        peak_src_note = f"{peak_src} BF16 burst x nominal FP8/BF16 ratio 2 (4.5 / 2.25 PF)"
+    else:
+        peak_src_note = f"{peak_src} BF16 burst x nominal FP16/BF16 ratio 1 (2.25 PF both)"
     roof.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
                  "traffic": traffic,
-                 "peak_source": (f"{peak_src} (burst)" if args.dtype == "bf16" or decode_cfg else
-                                 f"{peak_src} BF16 burst x nominal FP16/BF16 ratio 1 (2.25 PF both)"),
+                 "peak_source": peak_src_note,
                  "algorithmic_per_launch": a_bytes if decode_cfg else a_flops,
                  "kernel": "fa_fwd_kernel" if args.impl == "fused" else "naive (3 kernels)"})
 
@@ -920,8 +945,8 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step,
                 "note": ("fa_forward_host_packed: K requests in pinned host memory; libfa copies each in "
                          "and out on its own streams through two device slots, overlapping the "
-                         "neighbouring requests' kernels" if args.impl == "fused" else
-                         "unfused path: torch copies around each call, nothing overlapped"),
+                         "neighbouring requests' kernels" if args.impl == "fused" and args.dtype != "e4m3"
+                         else "torch copies around each call (pinned host buffers), nothing overlapped"),
                 "serial": e2e_serial},
         "gpu_launches": kernels_per_step * args.steps,
         "flushed": {"value": flushed_value, "unit": unit, "ms_per_step": flushed_ms / args.steps,

@@ -55,6 +55,7 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 _SIGNATURES = {
     "fa_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
     "fa_forward_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "fa_forward_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float] * 4 + [_vp]),
     "fa_forward_host": (_c_int, [_c_int] + [ctypes.POINTER(_vp)] * 5 + [_c_int] * 7 +
                         [_c_float, _c_int, _vp]),
     "fa_forward_host_packed": (_c_int, [_c_int] + [ctypes.POINTER(_vp)] * 2 + [_c_int] * 7 +
@@ -194,6 +195,35 @@ def fa_forward_fp16(q, k, v, causal: bool = False, scale: float | None = None, o
     st = lib().fa_forward_fp16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q,
                                N_k, d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "fa_forward_fp16")
+    return out, lse
+
+
+def fa_forward_fp8(q, k, v, descale, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                   return_lse: bool = True, stream=None):
+    """Fused forward on FP8 E4M3 inputs: q, k, v hold E4M3 codes (torch.uint8 or
+    torch.float8_e4m3fn, one byte each) standing for code * factor, with
+    ``descale = (factor_q, factor_k, factor_v)``. Returns ``(o, lse)``: o BF16,
+    lse FP32. d must be 128."""
+    import torch
+    allowed = {torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)}
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in allowed:
+            raise TypeError(f"{name} is {t.dtype}, expected E4M3 codes (torch.uint8 or torch.float8_e4m3fn)")
+    if out is not None and out.dtype != torch.bfloat16:
+        raise TypeError(f"out is {out.dtype}, expected torch.bfloat16")
+    if lse is not None and lse.dtype != torch.float32:
+        raise TypeError(f"lse is {lse.dtype}, expected torch.float32")
+    B, H_q, H_kv, N_q, N_k, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, N_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H_q, N_q), dtype=torch.float32, device=q.device)
+    dq, dk, dv = (float(x) for x in descale)
+    st = lib().fa_forward_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv, N_q, N_k,
+                              d, int(bool(causal)), float(scale), dq, dk, dv, _stream_ptr(stream))
+    _check(st, "fa_forward_fp8")
     return out, lse
 
 

@@ -69,7 +69,7 @@ int validate_shape(const Shape& s) {
 }
 
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const Shape& s, float scale, bool check_device) {
+             const Shape& s, float scale, bool check_device, int in_esz) {
   int st = validate_shape(s);
   if (st != FA_OK) return st;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -79,13 +79,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return FA_ERR_INVALID_ARG;
   if (rows_k > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
-  const size_t qb = (size_t)rows_q * s.d * 2, kb = (size_t)rows_k * s.d * 2;
+  const size_t qb = (size_t)rows_q * s.d * in_esz, kb = (size_t)rows_k * s.d * in_esz;
+  const size_t ob = (size_t)rows_q * s.d * 2;
   const size_t lb = lse ? (size_t)rows_q * 4 : 0;
   // outputs may not overlap any input or each other
-  if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb))
+  if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb))
     return FA_ERR_INVALID_ARG;
   if (lse && (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-              overlaps(lse, lb, o, qb)))
+              overlaps(lse, lb, o, ob)))
     return FA_ERR_INVALID_ARG;
   if (!check_device) return FA_OK;
   const void* ptrs[5] = {q, rows_k > 0 ? k : nullptr, rows_k > 0 ? v : nullptr, o, lse};
@@ -274,6 +275,20 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                     uint64_t outer, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -343,10 +358,23 @@ FwdPlan prefill_plan(int B, int H_q, int N_q, int N_k, int d, int causal) {
 
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t strm,
-                 const WorkspaceSource& wsrc, int elem, PairedLaunch paired) {
-  if (elem != 0 && elem != 1) return FA_ERR_INVALID_ARG;
+                 const WorkspaceSource& wsrc, int elem, PairedLaunch paired, const float* descale) {
+  if (elem != 0 && elem != 1 && elem != 2) return FA_ERR_INVALID_ARG;
+  const bool fp8 = elem == 2;
+  float qk_factor = 1.f, o_scale = 1.f;
+  if (fp8) {
+    if (!descale) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+      if (!std::isfinite(descale[i]) || !(descale[i] > 0.f)) return FA_ERR_INVALID_ARG;
+    qk_factor = descale[0] * descale[1];
+    o_scale = descale[2];
+    if (!std::isfinite(scale * qk_factor)) return FA_ERR_INVALID_ARG;
+  }
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
-  int st = validate(q, k, v, o, lse, s, scale);
+  int st = validate_shape(s);
+  if (st != FA_OK) return st;
+  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
+  st = validate(q, k, v, o, lse, s, scale, true, fp8 ? 1 : 2);
   if (st != FA_OK) return st;
   if ((long long)B * H_q * N_q == 0) return FA_OK;
   if (N_k == 0 || B * H_kv == 0) return fill_empty(o, lse, (long long)B * H_q * N_q, d, strm);
@@ -355,11 +383,14 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   if (!status) return cuda_fail(cudaGetLastError());
   const int G = H_q / H_kv;
   CUtensorMap tk, tv;
-  if (!make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
-      !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128))
+  if (fp8 ? (!make_tmap_u8_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, 128) ||
+             !make_tmap_u8_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, 128))
+          : (!make_tmap_bf16_3d(&tk, k, d, N_k, (uint64_t)B * H_kv, d, 128) ||
+             !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128)))
     return cuda_fail(cudaErrorInvalidValue);
 
-  if ((long long)G * N_q <= kDecodeMaxRows) {
+  // (FP8 inputs always take the prefill kernel, which handles any number of rows)
+  if (!fp8 && (long long)G * N_q <= kDecodeMaxRows) {
     // decode / few queries: every query row of a KV head fits one m16 MMA
     DecParams p{};
     p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
@@ -399,7 +430,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.kv_off = N_k - N_q;
   p.n_qb = (N_q + kBlockRows - 1) / kBlockRows;
   p.n_kv_tiles = (N_k + kTileN - 1) / kTileN;
-  p.c = scale * 1.4426950408889634f;
+  p.c = scale * qk_factor * 1.4426950408889634f;
+  p.o_scale = o_scale;
   p.o = o;
   p.lse = lse;
   p.status = status;
@@ -422,7 +454,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   maps.v = tv;
   // O boxes: a 128-row query tile, or the 256 / s rows one CTA of a cluster finishes
   const uint32_t o_box_rows = pl.cluster_merge ? (uint32_t)(kBlockRows / pl.s_tail) : 128u;
-  if (!make_tmap_bf16_3d(&maps.q, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
+  if (!(fp8 ? make_tmap_u8_3d(&maps.q, q, d, N_q, (uint64_t)B * H_q, 128)
+            : make_tmap_bf16_3d(&maps.q, q, d, N_q, (uint64_t)B * H_q, d, 128)) ||
       !make_tmap_bf16_3d(&maps.o, o, d, N_q, (uint64_t)B * H_q, d, o_box_rows))
     return cuda_fail(cudaErrorInvalidValue);
   if (multicast) {
@@ -536,6 +569,14 @@ int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float*
                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale, void* stream) {
   return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
                       static_cast<cudaStream_t>(stream), pool_workspace(), 1);
+}
+
+int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                   int H_kv, int N_q, int N_k, int d, int causal, float scale, float descale_q,
+                   float descale_k, float descale_v, void* stream) {
+  const float descale[3] = {descale_q, descale_k, descale_v};
+  return forward_impl(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, scale,
+                      static_cast<cudaStream_t>(stream), pool_workspace(), 2, nullptr, descale);
 }
 
 int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -74,20 +74,36 @@ constexpr int kRegsOther = 72;      // per thread, warpgroup 2
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 // A row's reference max may lag its true max by up to kTau (log2 units), so P
-// stays <= 2^kTau: 2^16 in BF16, 2^15 in FP16 (whose largest finite value is 65504).
+// stays <= 2^kTau: 2^16 in BF16, 2^15 in FP16 (whose largest finite value is
+// 65504), 2^8 in FP8 E4M3 (largest finite value 448).
 template <Elem E>
 struct Lag {
-  static constexpr float kTau = E == Elem::F16 ? 15.0f : 16.0f;
-  static constexpr float kSumCap = E == Elem::F16 ? 32768.0f : 65536.0f;   // 2^kTau
+  static constexpr float kTau = E == Elem::F16 ? 15.0f : (E == Elem::E4M3 ? 8.0f : 16.0f);
+  static constexpr float kSumCap = E == Elem::F16 ? 32768.0f : (E == Elem::E4M3 ? 256.0f : 65536.0f);
 };
+// Element type of O: the input type, except BF16 for FP8 inputs.
+template <Elem E>
+constexpr Elem kOutElem = E == Elem::E4M3 ? Elem::BF16 : E;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+template <int D, Elem E = Elem::BF16>
 struct Cfg {
-  static constexpr int kBoxes = D / 64;               // 64-column (128-byte) boxes per tile row
-  static constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 bytes
-  static constexpr int kTileBytes = 128 * D * 2;      // one Q, K or V tile (BF16)
-  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring depth
+  static constexpr int kEsz = E == Elem::E4M3 ? 1 : 2;   // bytes per Q, K, V element
+  static constexpr int kBoxCols = 128 / kEsz;             // elements in one 128-byte box row
+  static constexpr int kBoxes = D * kEsz / 128;           // 128-byte boxes per tile row
+  static_assert(kBoxes >= 1, "a tile row holds at least one 128-byte box");
+  static constexpr int kOBoxes = D / 64;                  // 64-column boxes of a 16-bit O row
+  static constexpr int kBoxBytes = 128 * 128;             // 128 rows x 128 bytes
+  static constexpr int kTileBytes = 128 * D * kEsz;       // one Q, K or V tile
+  static constexpr int kOTileBytes = 128 * D * 2;         // one 16-bit O tile
+  static constexpr int kPartTileBytes = 128 * D * 4;      // one FP32 partial tile
+  static constexpr int kStages = kTileBytes >= 32768 ? 4 : 8;   // K/V ring depth
+  // MMAs per tile: S = Q K^T takes 32 bytes of d per MMA (16 BF16/FP16 or 32 FP8
+  // elements); P V takes kPVKeys keys per MMA, 8 TMEM columns of P each
+  static constexpr int kSKSteps = D * kEsz / 32;
+  static constexpr int kPVKeys = 32 / kEsz;
+  // TMEM columns of one 64-key half of P (2 BF16/FP16 or 4 FP8 values per column)
+  static constexpr uint32_t kPHalfCols = 64 * kEsz / 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
@@ -109,6 +125,8 @@ struct Cfg {
   static constexpr int kCmStage = kBlockRows * D * 4;         // after the FP32 receive buffer
   static constexpr int kSmemBytes = kOffCm + kCmRows * 8 + 1024;  // + alignment slack
   static_assert(kCmStage + 128 * D * 2 <= kOffBar, "merge buffers must fit in the Q tiles and the K/V ring");
+  static_assert(2 * kPartTileBytes <= kStages * kTileBytes, "both partial tiles fit in the K/V ring");
+  static_assert(kEsz == 2 || 2 * kOTileBytes <= kStages * kTileBytes, "FP8: O staged in the K/V ring");
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory column of S_X / P_X and of O_X
   __device__ static constexpr uint32_t tm_s(int X) { return X ? 128u : 0u; }
@@ -119,10 +137,10 @@ __device__ __forceinline__ int min_i(int a, int b) { return a < b ? a : b; }
 __device__ __forceinline__ int max_i(int a, int b) { return a > b ? a : b; }
 
 // P = 2^(s*c - mb) for 64 scores of this thread's row (FP32 pairs, one packed
-// FMA per pair), packed to BF16 and stored to 32 TMEM columns from tP. Returns
-// the sum of P (FP32). Software-pipelined in chunks of 16: the exponentials of
-// chunk k+1 are issued before chunk k is packed and stored, so the exp unit
-// stays busy.
+// FMA per pair), packed to the P type (BF16 or FP16: 32 TMEM columns from tP;
+// FP8 E4M3: 16 columns). Returns the sum of P (FP32, before rounding).
+// Software-pipelined in chunks of 16: the exponentials of chunk k+1 are issued
+// before chunk k is packed and stored, so the exp unit stays busy.
 template <Elem E>
 __device__ __forceinline__ float exp_half(const float* s, float c, float mb, uint32_t tP) {
   float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
@@ -143,10 +161,17 @@ __device__ __forceinline__ float exp_half(const float* s, float c, float mb, uin
         pb[i + 1] = ex2_approx(e.y);
       }
     }
-    uint32_t pk[8];
+    if constexpr (E == Elem::E4M3) {
+      uint32_t pk[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pk[i] = pack2<E>(pa[2 * i], pa[2 * i + 1]);
-    tmem_st8(tP + (uint32_t)k * 8u, pk);
+      for (int i = 0; i < 4; ++i) pk[i] = pack4_e4m3(pa[4 * i], pa[4 * i + 1], pa[4 * i + 2], pa[4 * i + 3]);
+      tmem_st4(tP + (uint32_t)k * 4u, pk);
+    } else {
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pk[i] = pack2<E>(pa[2 * i], pa[2 * i + 1]);
+      tmem_st8(tP + (uint32_t)k * 8u, pk);
+    }
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
       sa = fadd2(sa, make_float2(pa[i], pa[i + 1]));
@@ -248,7 +273,7 @@ __device__ __forceinline__ void cm_send(uint32_t sb, uint32_t ml_base, int S, in
 template <int D, int S, Elem E>
 __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t stage, int w, int warp,
                                        int lane, bool ok, const FwdParams& p, const CUtensorMap* tmO,
-                                       int bh, int q0) {
+                                       int bh, int q0, float o_scale) {
   constexpr int kC = D / 4;               // FP32 chunks per row
   constexpr int kCB = D / 8;              // BF16 16-byte chunks per row
   constexpr int R = kBlockRows / S;
@@ -271,7 +296,7 @@ __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t s
     wv[v] = ls[v] > 0.f ? ex2_approx(ms[v] - M) : 0.f;
     L += wv[v] * ls[v];
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = L > 0.f ? o_scale / L : 0.f;
 #pragma unroll
   for (int v = 0; v < S; ++v) wv[v] *= inv;
   if ((item0 % kCB) == 0 && row < p.N_q && p.lse)
@@ -304,9 +329,10 @@ __device__ __noinline__ void cm_reduce(uint32_t sb, uint32_t ml_base, uint32_t s
         acc[6] += wv[v] * t[q][v][1].z; acc[7] += wv[v] * t[q][v][1].w;
       }
       const int bx = cb >> 3, cbb = cb & 7;
+      constexpr Elem OE = kOutElem<E>;
       st_shared_v4(stage + (uint32_t)(bx * R + lr) * 128u + ((uint32_t)(cbb ^ (lr & 7)) << 4),
-                   pack2<E>(acc[0], acc[1]), pack2<E>(acc[2], acc[3]), pack2<E>(acc[4], acc[5]),
-                   pack2<E>(acc[6], acc[7]));
+                   pack2<OE>(acc[0], acc[1]), pack2<OE>(acc[2], acc[3]), pack2<OE>(acc[4], acc[5]),
+                   pack2<OE>(acc[6], acc[7]));
     }
   }
   fence_proxy_async_smem();
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const __grid_constant__ CUtensorMap tmP, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -496,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_3d(sb + C::kOffQ + X * C::kTileBytes + bx * C::kBoxBytes, &tmQ, bar(C::kBarQ),
-                      bx * 64, q0 + X * kTileM, bh);
+                      bx * C::kBoxCols, q0 + X * kTileM, bh);
     }
   }
   if (warp == kWarpMma) {
@@ -536,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!MC) {
 #pragma unroll
               for (int bx = 0; bx < C::kBoxes; ++bx)
-                tma_load_3d_hint(dst + bx * C::kBoxBytes, tmap, bar(C::kBarFull + st), bx * 64,
+                tma_load_3d_hint(dst + bx * C::kBoxBytes, tmap, bar(C::kBarFull + st), bx * C::kBoxCols,
                                  tile * kTileN, bhk, pol);
             } else if (share) {
               // this CTA's half of the rows, into both CTAs
@@ -591,25 +617,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lq0 = desc_sw128_lo(sb + C::kOffQ, 16);
         const uint32_t lk0 = desc_sw128_lo(sb + C::kOffKV, 16);
         const uint32_t lv0 = desc_sw128_lo(sb + C::kOffKV, C::kBoxBytes);
+        // MMA kk of S covers bytes 32kk .. 32kk+31 of each 128-byte box row
         auto issue_S = [&](int X, int st) {
           const uint32_t a0 = lq0 + (uint32_t)X * kStageStep;
           const uint32_t b0 = lk0 + (uint32_t)st * kStageStep;
           const uint32_t d = tmem + C::tm_s(X);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < C::kSKSteps; ++kk) {
             constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
             const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
-            mma_ss_lh_w(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
+            if constexpr (E == Elem::E4M3)
+              mma_ss_lh_w_f8(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
+            else
+              mma_ss_lh_w(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
           }
         };
+        // MMA kk of P V takes keys kPVKeys*kk .. (P in TMEM columns 8kk .. 8kk+7,
+        // V rows from kPVKeys*kk on, 128 bytes each)
         auto issue_PV = [&](int X, int st, bool acc, int h) {   // keys 64h .. 64h+63
+          constexpr int kPer = 64 / C::kPVKeys;
+          constexpr uint32_t kVStep = (uint32_t)(C::kPVKeys * 128) >> 4;
           const uint32_t b0 = lv0 + (uint32_t)st * kStageStep;
           const uint32_t d = tmem + C::tm_o(X);
           const uint32_t a = tmem + C::tm_s(X);
 #pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // P of keys 16kk .. 16kk+15 in columns 8kk ..
-            mma_ts_lh_w(d, a + (uint32_t)kk * 8u,
-                      b0 + (uint32_t)kk * (16u * 128u >> 4), kHi, idO, (acc || kk > 0) ? 1u : 0u);
+          for (int kk = kPer * h; kk < kPer * h + kPer; ++kk) {
+            if constexpr (E == Elem::E4M3)
+              mma_ts_lh_w_f8(d, a + (uint32_t)kk * 8u, b0 + (uint32_t)kk * kVStep, kHi, idO,
+                             (acc || kk > 0) ? 1u : 0u);
+            else
+              mma_ts_lh_w(d, a + (uint32_t)kk * 8u, b0 + (uint32_t)kk * kVStep, kHi, idO,
+                          (acc || kk > 0) ? 1u : 0u);
+          }
         };
         bool ok = mbar_wait_w(bar(C::kBarQ), 0, s_abort, p.status);
         if (ok) ok = mbar_wait_w(bar(C::kBarFull + 0), 0, s_abort, p.status);
@@ -719,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mb = m_ref == -INFINITY ? 0.f : m_ref;
         const float r1 = exp_half<E>(s, c, mb, tS);
         publish(bar(C::kBarP1 + X));
-        const float r2 = exp_half<E>(s + 64, c, mb, tS + 32);
+        const float r2 = exp_half<E>(s + 64, c, mb, tS + C::kPHalfCols);
         publish(bar(C::kBarP2 + X));
         l += r1 + r2;
       } else {
@@ -741,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         publish(bar(C::kBarP1 + X));
         // the second half's P <= 2^kTau now
-        const float r2 = exp_half<E>(s + 64, c, m_ref, tS + 32);
+        const float r2 = exp_half<E>(s + 64, c, m_ref, tS + C::kPHalfCols);
         publish(bar(C::kBarP2 + X));
         l += r1 + r2;
       }
@@ -762,16 +801,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cluster_sync();   // all partials of this CTA's rows have landed
       {
         const uint32_t rb = sb + C::kOffQ, mb2 = sb + C::kOffCm, stg = sb + C::kOffQ + C::kCmStage;
-        if (p.s_tail == 2) cm_reduce<D, 2, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
-        else if (p.s_tail == 4) cm_reduce<D, 4, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
-        else cm_reduce<D, 8, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0);
+        const float os = p.o_scale;
+        if (p.s_tail == 2) cm_reduce<D, 2, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0, os);
+        else if (p.s_tail == 4) cm_reduce<D, 4, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0, os);
+        else cm_reduce<D, 8, E>(rb, mb2, stg, ui.split, warp, lane, ok, p, &tmO, bh, q0, os);
       }
     } else if (slot < 0) {
       // ---- final epilogue: O / l -> BF16 into this tile's Q slot (128-byte
       // swizzled boxes, the tensor map's layout), then one TMA store; LSE direct
-      const uint32_t obase = sb + C::kOffQ + X * C::kTileBytes;
+      // (FP8 inputs: the BF16 O tile is twice a Q tile, staged in the idle K/V ring)
+      const uint32_t obase = E == Elem::E4M3 ? sb + C::kOffKV + X * C::kOTileBytes
+                                             : sb + C::kOffQ + X * C::kTileBytes;
+      constexpr Elem OE = kOutElem<E>;
       if (ok) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? p.o_scale / l : 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           float ov[32];
@@ -787,10 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < 4; ++g) {
             const uint32_t ch = (uint32_t)(((cc & 63) >> 3) + g);   // 16-byte chunk in the row
             st_shared_v4(rowaddr + ((ch ^ (uint32_t)(r & 7)) << 4),
-                         pack2<E>(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
-                         pack2<E>(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
-                         pack2<E>(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
-                         pack2<E>(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
+                         pack2<OE>(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
+                         pack2<OE>(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
+                         pack2<OE>(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
+                         pack2<OE>(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
           }
         }
         if (valid_row && p.lse)
@@ -800,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool all_ok = named_bar_and(1 + X, 128, ok);
       if (all_ok && r == 0 && tile_first_row < p.N_q) {   // rows past N_q are clipped by the TMA
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
+        for (int bx = 0; bx < C::kOBoxes; ++bx)
           tma_store_3d(&tmO, obase + bx * C::kBoxBytes, bx * 64, tile_first_row, bh);
         bulk_commit();
         bulk_wait_read0();
@@ -808,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ---- partial: unnormalised O (FP32, 32-column swizzled boxes staged in the
       // K/V ring, one TMA store) and (m, l) of this key range to the workspace
-      const uint32_t pbase = sb + C::kOffKV + X * 2 * C::kTileBytes;
+      const uint32_t pbase = sb + C::kOffKV + X * C::kPartTileBytes;
       const int prow0 = slot * kBlockRows + X * kTileM;
       if (ok) {
 #pragma unroll 1
@@ -906,7 +949,7 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
   float L = w * l;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = L > 0.f ? p.o_scale / L : 0.f;
   float acc[kCols];
 #pragma unroll
   for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
@@ -921,13 +964,14 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const FwdParams p) {
     }
   }
   uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)bh * p.N_q + row) * D;   // 16-bit elements
+  constexpr Elem OE = kOutElem<E>;
   if constexpr (kCols == 4) {
     uint2 v;
-    v.x = pack2<E>(acc[0], acc[1]);
-    v.y = pack2<E>(acc[2], acc[3]);
+    v.x = pack2<OE>(acc[0], acc[1]);
+    v.y = pack2<OE>(acc[2], acc[3]);
     *reinterpret_cast<uint2*>(orow + lane * 4) = v;
   } else {
-    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack2<E>(acc[0], acc[1]);
+    *reinterpret_cast<uint32_t*>(orow + lane * 2) = pack2<OE>(acc[0], acc[1]);
   }
   if (lane == 0 && p.lse) p.lse[(size_t)bh * p.N_q + row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
@@ -940,7 +984,7 @@ cudaError_t ensure_smem_attr() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (attr[dev]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MC, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<D>::kSmemBytes);
+                                       Cfg<D, E>::kSmemBytes);
   if (e == cudaSuccess) attr[dev] = true;
   return e;
 }
@@ -951,7 +995,7 @@ int cluster_capacity_t(int s) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)s);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<D, Elem::BF16>::kSmemBytes;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = (unsigned)s;
@@ -960,7 +1004,7 @@ int cluster_capacity_t(int s) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  // the FP16 kernel has the same resources: one answer serves both
+  // the FP16 and FP8 kernels also run one CTA per SM: one answer serves all three
   if (cudaOccupancyMaxActiveClusters(&n, fa_fwd_kernel<D, false, Elem::BF16>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -977,7 +1021,7 @@ cudaError_t launch_main_t(const FwdMaps& m, const FwdParams& p, int units, cudaS
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(MC ? ((units + 1) & ~1) : units));   // MC: whole clusters of two
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<D, E>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -28,9 +28,10 @@ struct FwdParams {
   int s_tail;       // ... into s_tail key ranges each (units u_full + t*s_tail + s)
   int n_units;      // work units (the grid may hold one more, idle, CTA to complete a cluster)
   int cm;           // 1: every block is split and its s_tail CTAs (one cluster) merge in-kernel
-  int elem;         // element type of Q, K, V, O: 0 = BF16, 1 = FP16 (host-side dispatch)
-  float c;          // scale * log2(e)
-  void* o;          // bf16 [B][H_q][N_q][d]
+  int elem;         // element type of Q, K, V: 0 = BF16, 1 = FP16 (O the same), 2 = FP8 E4M3 (O BF16)
+  float c;          // scale * log2(e) (FP8: times the Q and K factors)
+  float o_scale;    // factor on the normalised output: 1, or the V factor of FP8 inputs
+  void* o;          // 16-bit [B][H_q][N_q][d]
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
   float* part_o;    // fp32 [n_tail*s_tail][kBlockRows][d]        (n_tail > 0)
   float* part_ml;   // fp32 [n_tail*s_tail][kBlockRows][2] (m, l)  (n_tail > 0)
@@ -136,8 +137,9 @@ struct Shape {
 int validate_shape(const Shape& s);
 // Argument checks shared by the forward entry points (fa_status code; FA_OK when valid);
 // check_device: also require every pointer to be memory of the current device.
+// in_esz: bytes per element of q, k, v (2, or 1 for FP8; o is always 16-bit).
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const Shape& s, float scale, bool check_device = true);
+             const Shape& s, float scale, bool check_device = true, int in_esz = 2);
 // O = 0 and LSE = -inf for `rows` rows (every row sees no key).
 int fill_empty(void* o, float* lse, long long rows, int d, cudaStream_t st);
 // Record a CUDA error for fa_get_last_cuda_error and return FA_ERR_CUDA; the
@@ -163,6 +165,9 @@ extern thread_local int g_last_cuda_error;
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);
+// 3-D 8-bit tensor map over [outer][rows][inner] with a {128, box_rows, 1} box, 128-byte swizzle.
+bool make_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                     uint64_t outer, uint32_t box_rows);
 
 // 2-D FP32 tensor map over [rows][inner] with a {32, 128} box, 128-byte swizzle.
 bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows);
@@ -181,9 +186,11 @@ const WorkspaceSource& pool_workspace();   // library-owned stream-ordered pool
 // elem: 0 = BF16, 1 = FP16 tensors.
 // paired: the paired-load launcher, used for BF16 plans without split tails
 // (nullptr: the plain kernel always).
+// elem 2 (FP8 E4M3): descale = the Q, K, V factors (else ignored).
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
                  int H_kv, int N_q, int N_k, int d, int causal, float scale, cudaStream_t stream,
-                 const WorkspaceSource& ws, int elem = 0, PairedLaunch paired = nullptr);
+                 const WorkspaceSource& ws, int elem = 0, PairedLaunch paired = nullptr,
+                 const float* descale = nullptr);
 // Every non-null pointer is device memory of the current device (FA_OK),
 // else FA_ERR_INVALID_ARG; FA_ERR_CUDA when the device cannot be queried.
 int check_current_device(const void* const* ptrs, int n);

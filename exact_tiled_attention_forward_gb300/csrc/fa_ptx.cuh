@@ -305,6 +305,32 @@ __device__ __forceinline__ void mma_ts_lh_w(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// kind::f8f6f4 forms (8-bit A and B, FP32 accumulator; K = 32 per MMA), same
+// warp-converged issue as above.
+__device__ __forceinline__ void mma_ss_lh_w_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b64 ad, bd;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "mov.b64 ad, {%1, %2};\n\t"
+      "mov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lh_w_f8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b64 bd;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
@@ -350,6 +376,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns store.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
 }
 
 // 32 lanes x 8 consecutive 32-bit columns store.
@@ -400,13 +433,16 @@ __device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_b
   return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
 
-// 16-bit element type of Q, K, V, P and O (FP32 accumulation either way).
-enum class Elem : int { BF16 = 0, F16 = 1 };
+// Element type of Q, K, V and P (FP32 accumulation either way): BF16 or FP16
+// (O in the same type), or FP8 E4M3 codes with per-tensor factors (O in BF16).
+enum class Elem : int { BF16 = 0, F16 = 1, E4M3 = 2 };
 
-// Instruction descriptor, kind::f16: 16-bit x 16-bit -> FP32, dense.
-//   bits 4-5 D format (1 = F32), 7-9 A format and 10-12 B format (0 = F16, 1 = BF16;
-//   A and B always the same type here), bit 15 A major (0 = K), bit 16 B major
-//   (1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
+// Instruction descriptor, kind::f16 (16-bit x 16-bit) or kind::f8f6f4 (8-bit x
+// 8-bit) -> FP32, dense.
+//   bits 4-5 D format (1 = F32), 7-9 A format and 10-12 B format (kind::f16:
+//   0 = F16, 1 = BF16; kind::f8f6f4: 0 = E4M3; A and B always the same type
+//   here), bit 15 A major (0 = K), bit 16 B major (1 = MN), bits 17-22 N >> 3,
+//   bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f32(int M, int N, bool b_mn_major, Elem e = Elem::BF16) {
   return (1u << 4) | ((e == Elem::BF16 ? 1u : 0u) << 7) | ((e == Elem::BF16 ? 1u : 0u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -424,11 +460,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-// Two FP32 values rounded (to nearest even) to the element type, low half first.
+// Two FP32 values rounded (to nearest even) to the 16-bit type, low half first
+// (E4M3 inputs produce BF16 outputs).
 template <Elem E>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (E == Elem::F16) return pack_f16x2(lo, hi);
   else return pack_bf16x2(lo, hi);
+}
+// Four FP32 values rounded to nearest even into FP8 E4M3 codes, saturating at
+// +-448, first value in the lowest byte (the k order of a tcgen05 A operand).
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  // cvt ... x2 d, x, y puts y in the low byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -7,8 +7,8 @@
  * Also returned: the FP32 log-sum-exp of each row's scaled scores, the small
  * per-row statistic the backward pass recomputes from. Around the forward:
  * its backward pass (fa_backward), decode over a paged K/V cache
- * (fa_decode_paged), FP16 tensors, host-memory requests, an allocation-free
- * variant and the unfused baseline.
+ * (fa_decode_paged), FP16 tensors, FP8 E4M3 inputs (fa_forward_fp8),
+ * host-memory requests, an allocation-free variant and the unfused baseline.
  *
  * Sources: "Why is standard attention memory-bound, and how does FlashAttention
  * fix it?" (interview.clozo.ai), Step 1 (definition), Step 3 (online softmax),
@@ -36,7 +36,7 @@
  *    key gets O = 0 and LSE = -inf.
  *  - lse[i] = ln(sum_j exp(scale * q_i . k_j)) over the visible keys.
  *  - scale must be finite and > 0 (1/sqrt(d) is the usual value).
- *  - d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ *  - d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise; 128 for FP8 inputs).
  *  - stream: a cudaStream_t (NULL = legacy default stream). Calls are
  *    asynchronous: they return once the work is enqueued. Argument errors are
  *    reported before anything is enqueued. Launch errors return FA_ERR_CUDA
@@ -101,6 +101,24 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int H_q, int H_kv, int N_q, int N_k, int d, int causal, float scale,
                     void* stream);
+
+/* fa_forward on FP8 inputs ("Flash Attention Mechanics...", "FlashAttention 2
+ * and FlashAttention 3": FP8 as the next precision step). q, k, v hold FP8
+ * E4M3 codes (one byte per element: sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, subnormals, no infinities, 0x7F/0xFF NaN), in fa_forward's
+ * layouts; each tensor stands for decode(code) * its factor (descale_q,
+ * descale_k, descale_v: finite and > 0). The result is attention over those
+ * values: o is BF16 [B][H_q][N_q][d], lse FP32 [B][H_q][N_q] as in fa_forward.
+ * Arithmetic: S = Q K^T from the codes on the tensor cores (exact products,
+ * FP32 accumulation), the factors of Q and K and `scale` folded into the
+ * exponent; P rounded to E4M3 (nearest even, at most 2^8 against the row's
+ * reference max) for the P V product; O multiplied by descale_v / l in FP32
+ * and rounded to BF16. d must be 128 (FA_ERR_UNSUPPORTED otherwise). Every
+ * request runs the prefill kernel (including one-query decode shapes). Pointers,
+ * alignment, overlap, workspace and error codes as fa_forward. */
+int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                   int H_kv, int N_q, int N_k, int d, int causal, float scale, float descale_q,
+                   float descale_k, float descale_v, void* stream);
 
 /* n forward requests of one shape whose tensors live in HOST memory (no
  * counterpart on the pages, which start from tensors in device memory: this is

@@ -19,8 +19,9 @@ Contents
                finite differences of the forward).
 ``paged``      decode over a paged K/V cache: each sequence's keys read out of
                its pages in order, then the definition.
-``fp8``        FP8 E4M3 inputs: the exact value of each code, and the definition
-               on code * per-tensor factor.
+``fp8``        FP8 E4M3 inputs: the exact value of each code, the definition
+               on code * per-tensor factor, and the most that rounding P to
+               E4M3 can move each output (the FP8 path's error term).
 
 Every function names the page and section it follows. Each is pinned in
 ``tests/test_oracle_*.py`` against values the pages print, closed forms and
@@ -40,4 +41,4 @@ from .attention import (  # noqa: F401
 from . import traffic  # noqa: F401
 from .backward import attention_backward, backward_error_terms, forward_loss  # noqa: F401
 from .paged import gather_sequence, paged_attention_reference  # noqa: F401
-from .fp8 import attention_reference_fp8, e4m3_to_f64  # noqa: F401
+from .fp8 import attention_reference_fp8, e4m3_to_f64, p_rounding_bound_fp8, p_rounding_weight  # noqa: F401

@@ -68,6 +68,23 @@ def bf16_dev_to_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+# FP8 E4M3 inputs (fa_forward_fp8): the inputs are exact E4M3 values and S is
+# exact up to FP32 accumulation, so the only rounding of note is P's, to E4M3,
+# before the P V product: oracle.p_rounding_bound_fp8 gives E, the most it can
+# move each output for any reference max the kernel holds (P <= 2^8). O is
+# rounded to BF16 at the end:
+#   |dO| <= max(1e-2, half_spacing_bf16(|O_ref| + E') + E'),  E' = E + 2^-16 A
+# The relative L2 error is held to E4M3's unit roundoff 2^-4 (a weighted sum of
+# values each off by at most that relative amount in the normal range); the LSE
+# involves no FP8 rounding and keeps the stated 1e-3.
+TOL_REL_L2_O_FP8 = 2.0 ** -4
+
+
+def elementwise_bound_fp8(o_ref, a_ref, e_ref, floor=TOL_MAX_ABS_O):
+    e = np.asarray(e_ref, dtype=np.float64) + U_ACC * np.asarray(a_ref, dtype=np.float64)
+    return np.maximum(floor, half_spacing(np.abs(np.asarray(o_ref, dtype=np.float64)) + e, "bf16") + e)
+
+
 def _log_parity(res):
     """Append this comparison's figures to $FA_PARITY_LOG (JSON lines) if set."""
     import json
@@ -80,11 +97,12 @@ def _log_parity(res):
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
-            tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE, elem="bf16"):
+            tol_rel=TOL_REL_L2_O, tol_lse=TOL_MAX_ABS_LSE, elem="bf16", fp8_e=None):
     """Element-wise comparison of O and LSE; returns a dict of error figures,
     including how many elements of O differ by more than the stated 1e-2
     (``n_over_1e2``) and the largest |O_ref| among them. ``o_abs_ref`` is A (the
-    oracle's attention of |V|); ``elem`` ("bf16" or "f16") the element type."""
+    oracle's attention of |V|); ``elem`` ("bf16", "f16" or "e4m3") the input
+    type; ``fp8_e`` the oracle's P-rounding term for "e4m3"."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape
@@ -92,7 +110,10 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
     err = np.abs(o_gpu - o_ref)
     max_abs = float(err.max()) if err.size else 0.0
     a_ref = np.abs(o_ref) if o_abs_ref is None else np.asarray(o_abs_ref, dtype=np.float64)
-    bound = elementwise_bound(o_ref, a_ref, elem, floor=tol_o)
+    if elem == "e4m3":
+        bound = elementwise_bound_fp8(o_ref, a_ref, fp8_e, floor=tol_o)
+    else:
+        bound = elementwise_bound(o_ref, a_ref, elem, floor=tol_o)
     worst = float((err / bound).max()) if err.size else 0.0
     over = err > TOL_MAX_ABS_O
     denom = float(np.linalg.norm(o_ref))
@@ -113,6 +134,17 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, o_abs_ref=None, tol_o=TOL_MAX_ABS_O,
     assert worst <= 1.0, res
     assert rel <= tol_rel, res
     return res
+
+
+def run_oracle_fp8(a):
+    """(O, LSE, A, E) for FP8 inputs: the oracle on the decoded values, A on
+    |V|, and E = oracle.p_rounding_bound_fp8."""
+    from oracle.fp8 import attention_reference_fp8, p_rounding_bound_fp8
+    o, lse = attention_reference_fp8(a.q, a.k, a.v, a.descale, causal=a.causal, scale=a.scale)
+    v_abs = a.v & np.uint8(0x7F)                 # |code|: the sign bit cleared
+    o_abs, _ = attention_reference_fp8(a.q, a.k, v_abs, a.descale, causal=a.causal, scale=a.scale)
+    e = p_rounding_bound_fp8(a.q, a.k, a.v, a.descale, causal=a.causal, scale=a.scale)
+    return o, lse, o_abs, e
 
 
 def run_oracle(a):

@@ -25,7 +25,8 @@ def lib():
 
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
-    assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_host", "fa_forward_host_packed",
+    assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_fp8", "fa_forward_host",
+                          "fa_forward_host_packed",
                           "fa_backward", "fa_decode_paged",
                           "fa_forward_noalloc",
                           "fa_naive_forward",
@@ -126,6 +127,21 @@ def test_noalloc_rejects_like_forward(lib):
     assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 96, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
     assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
     assert f(0, 0, 0, 0, 0, 1, 2, 1, 0, 64, 128, 0, 0.1, None) == fa.FA_OK
+
+
+def test_fp8_rejects(lib):
+    def f(q=Q, k=K, v=V, o=O, l=L, Hq=2, Hkv=1, Nq=64, d=128, scale=0.1, ds=(1.0, 1.0, 1.0)):
+        return lib.fa_forward_fp8(q, k, v, o, l, 1, Hq, Hkv, Nq, 64, d, 0, scale, *ds, None)
+    assert f(Hq=3, Hkv=2) == fa.FA_ERR_INVALID_ARG                       # H_q % H_kv
+    assert f(d=64) == fa.FA_ERR_UNSUPPORTED                               # FP8: d = 128 only
+    for bad in ((0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, math.inf), (1.0, math.nan, 1.0)):
+        assert f(ds=bad) == fa.FA_ERR_INVALID_ARG                         # factors finite, > 0
+    assert f(ds=(1e30, 1e30, 1.0)) == fa.FA_ERR_INVALID_ARG                # scale * factors overflows
+    # o (BF16, 2 bytes per element) may not overlap q (1 byte per element): q spans
+    # 2 * 64 * 128 bytes, so o may start right after it but not inside it
+    assert f(o=Q + 64 * 128) == fa.FA_ERR_INVALID_ARG
+    assert f(o=Q + 2 * 64 * 128) != fa.FA_ERR_INVALID_ARG
+    assert f(q=0, k=0, v=0, o=0, l=0, Nq=0) == fa.FA_OK
 
 
 def test_fp16_rejects_like_forward(lib):

@@ -8,6 +8,8 @@ import pytest
 import oracle
 from exact_tiled_attention_forward_gb300 import inputs as I
 
+from oracle.fp8 import attention_reference_fp8, e4m3_to_f64
+
 ALL = np.arange(256, dtype=np.uint8)
 
 
@@ -104,3 +106,67 @@ def test_fp8_reference_invariants():
     x = [oracle.e4m3_to_f64(c) * s for c, s in zip((a.q, a.k, a.v), a.descale)]
     o4, lse4 = oracle.attention_reference(*x, causal=True, scale=a.scale)
     assert np.array_equal(o4, o) and np.array_equal(lse4, lse)
+
+
+# ---- the FP8 path's P-rounding term (oracle.p_rounding_weight / p_rounding_bound_fp8)
+
+def test_p_rounding_weight_covers_every_reference_max():
+    # E4M3 rounding of lam * p, for lam anywhere in [1, 2^8] (the kernel's lag),
+    # changes it by at most lam * w(p); and the bound is reached
+    from oracle.fp8 import p_rounding_weight
+    p = np.concatenate([np.geomspace(2.0 ** -20, 1.0, 4001), [2.0 ** -6, 2.0 ** -10, 1.0]])
+    worst = 0.0
+    for lam in np.concatenate([2.0 ** np.arange(0, 9), np.geomspace(1.0, 256.0, 37)]):
+        x = lam * p
+        err = np.abs(e4m3_to_f64(I.f64_to_e4m3(x)) - x) / lam
+        w = p_rounding_weight(p)
+        assert np.all(err <= w * (1 + 1e-12)), lam
+        worst = max(worst, float((err / w).max()))
+    assert worst > 0.95
+
+
+def _simulate_fp8(a, p_mant_bits):
+    """O with the exact scores, P (against the true row max) rounded to E4M3, or
+    to fewer mantissa bits when p_mant_bits < 3 (a planted mistake)."""
+    from oracle.fp8 import e4m3_to_f64 as dec
+    sq, sk, sv = a.descale
+    q, k, v = dec(a.q)[0, 0] * sq, dec(a.k)[0, 0] * sk, dec(a.v)[0, 0] * sv
+    s = a.scale * q @ k.T
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    l = p.sum(axis=1, keepdims=True)
+    pr = dec(I.f64_to_e4m3(p))
+    if p_mant_bits < 3:
+        m, e = np.frexp(pr)
+        step = 2.0 ** (p_mant_bits + 1)
+        pr = np.ldexp(np.round(m * step) / step, e)
+    return (pr @ v) / l
+
+
+# (rows that sit on one or two scaled keys reach the bound; spread rows average
+# their rounding errors out, so the planted mistake shows only on the former)
+@pytest.mark.parametrize("n,frac,scale,seed,concentrated", [(256, 0.0, None, 3, False),
+                                                          (1024, 0.02, 0.3, 5, True)])
+def test_p_rounding_bound_holds_and_is_tight(n, frac, scale, seed, concentrated):
+    from oracle.fp8 import p_rounding_bound_fp8
+    a = I.make_inputs(1, 1, 1, n, n, 128, causal=False, seed=seed, k_row_frac=frac, scale=scale,
+                      dtype="e4m3")
+    o_ref, _ = attention_reference_fp8(a.q, a.k, a.v, a.descale, scale=a.scale)
+    bound = p_rounding_bound_fp8(a.q, a.k, a.v, a.descale, scale=a.scale)[0, 0]
+    ratio = np.abs(_simulate_fp8(a, 3) - o_ref[0, 0]) / bound
+    assert ratio.max() <= 1.0
+    assert ratio.max() >= (0.9 if concentrated else 0.15)
+    if concentrated:
+        # a planted mistake: P kept with one mantissa bit fewer than E4M3 has
+        planted = np.abs(_simulate_fp8(a, 2) - o_ref[0, 0]) / bound
+        assert planted.max() > 1.0
+
+
+def test_p_rounding_bound_masks_like_the_definition():
+    # causal: row i's bound uses keys 0..i only; a row that sees no key has 0
+    from oracle.fp8 import p_rounding_bound_fp8
+    a = I.make_inputs(1, 2, 1, 40, 24, 128, causal=True, seed=2, dtype="e4m3")
+    full = p_rounding_bound_fp8(a.q, a.k, a.v, a.descale, causal=True, scale=a.scale)
+    assert np.all(full[:, :, :16] == 0.0)            # N_q > N_k: rows 0..15 see no key
+    # row 16 sees key 0 only: p = 1, weight 2^-4, l = 1
+    v0 = np.abs(e4m3_to_f64(a.v[0, 0, 0]) * a.descale[2])
+    assert np.allclose(full[0, 0, 16], 2.0 ** -4 * v0, rtol=1e-12)
