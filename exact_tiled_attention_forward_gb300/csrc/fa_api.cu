@@ -64,7 +64,7 @@ int validate_shape(const Shape& s) {
   const long long rows_q = (long long)s.B * s.H_q * s.N_q;
   const long long rows_k = (long long)s.B * s.H_kv * s.N_k;
   if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-  if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
+  if (s.d != 64 && s.d != 128 && s.d != 256) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -389,6 +389,28 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
              !make_tmap_bf16_3d(&tv, v, d, N_k, (uint64_t)B * H_kv, d, 128)))
     return cuda_fail(cudaErrorInvalidValue);
 
+  if (d == 256) {
+    // one 128-row query tile per CTA; every query row takes this kernel
+    D256Params p{};
+    p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+    p.causal = causal ? 1 : 0;
+    p.kv_off = N_k - N_q;
+    p.n_qt = (N_q + 127) / 128;
+    p.n_kv_tiles = (N_k + 127) / 128;
+    p.elem = elem;
+    p.c = scale * 1.4426950408889634f;
+    p.lse = lse;
+    p.status = status;
+    const long long units = (long long)B * H_q * p.n_qt;
+    if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    CUtensorMap tq, to;
+    if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
+        !make_tmap_bf16_3d(&to, o, d, N_q, (uint64_t)B * H_q, d, 128))
+      return cuda_fail(cudaErrorInvalidValue);
+    cudaError_t e = launch_fwd_d256(tq, tk, tv, to, p, (int)units, strm);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
+
   // (FP8 inputs always take the prefill kernel, which handles any number of rows)
   if (!fp8 && (long long)G * N_q <= kDecodeMaxRows) {
     // decode / few queries: every query row of a KV head fits one m16 MMA
@@ -534,6 +556,9 @@ int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causa
   } else if (N_k == 0) {
     c = 256;   // O = 0, LSE = -inf fill
     n = 1;
+  } else if (d == 256) {
+    c = (long long)B * H_q * ((N_q + 127) / 128);   // one CTA per 128-row query tile
+    n = 1;
   } else if ((long long)(H_q / H_kv) * N_q <= fa::kDecodeMaxRows) {
     const int chunks = (N_k + 127) / 128;
     const fa::DecPlan dp = fa::decode_plan((long long)B * H_kv, chunks, d, fa::num_sms(),
@@ -585,6 +610,7 @@ int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
   int st = validate(q, k, v, o, lse, s, scale, false);
   if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;   // the unfused baseline covers d = 64 and 128
   if ((long long)B * H_q * N_q == 0) return FA_OK;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   if (N_k == 0) {

@@ -691,6 +691,7 @@ int backward_impl(const void* q, const void* k, const void* v, const void* o, co
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
   int st = validate_shape(s);
   if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;   // the backward kernels cover d = 64 and 128
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   const long long rows_q = (long long)B * H_q * N_q, rows_k = (long long)B * H_kv * N_k;
   const size_t qb = (size_t)rows_q * d * 2, kb = (size_t)rows_k * d * 2;

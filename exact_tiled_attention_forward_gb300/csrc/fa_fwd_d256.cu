@@ -1,0 +1,422 @@
+// Fused exact attention forward for head dimension 256 (BF16 or FP16 tensors).
+//
+// Same method as the d = 64 / 128 kernel ("Flash Attention Mechanics", "The
+// Tiling Algorithm"; "Why is standard attention memory-bound...", Step 3): a
+// CTA owns query rows, sweeps its key tiles with a running row max and sum,
+// rescales the partial output when the max rises, divides by the sum at the
+// end; scores live only in tensor memory. The tile plan differs because tensor
+// memory holds 512 FP32 columns per SM ("SRAM Constraints and Block Size
+// Selection": the block size follows the on-chip budget, which here is TMEM):
+// a d = 256 output tile takes 256 columns, so one 128-row query tile per CTA
+// with two 128-key score buffers ping-ponged instead of two query tiles:
+//   TMEM [0,128) S_0   [128,256) S_1   [256,512) O
+// The tensor core computes S(j+1) while the softmax warps turn S(j) into P(j),
+// then P(j) V, then S(j+2), ...: MMA issue order S(0), S(1), PV(0), S(2), PV(1),
+// S(3), ... keeps the pipe busy while one softmax runs (a tile's two products
+// take 2 x 1024 MMA cycles, its softmax well under that).
+//
+// Shared memory: the Q tile (128 rows x 256 columns, 64 KB, four 64-column
+// boxes with 128-byte swizzle) and a ring of five 32 KB stages, each one d-half
+// (128 columns) of a K or V tile: 64 + 160 KB. K and V of key tile j take two
+// stages each, loaded in the order the MMAs use them (K_0, K_1, V_0, K_2, V_1,
+// K_3, ...).
+//
+// Threads: warpgroup 0 (warps 0-3) runs the softmax and epilogue, one thread
+// per query row (TMEM lane); warp 4 issues TMA loads; warp 5 allocates TMEM and
+// issues the tcgen05 MMAs (one elected lane, warp converged); warps 6-7 idle.
+// P (16-bit) overwrites the first 64 columns of its S buffer and is the A
+// operand of the P V product straight from tensor memory. A row's reference
+// max lags its true max by at most tau (16 in BF16, 15 in FP16, log2 units) so
+// P stays finite in the element type; when a tile raises it, O is rescaled in
+// TMEM after P V of the previous tile has completed.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kD = 256;
+constexpr int kThreads256 = 256;
+constexpr int kWarpLoad = 4;
+constexpr int kWarpIssue = 5;
+constexpr int kStagesD = 5;
+constexpr int kHalfBytes = 128 * 128 * 2;   // one d-half of a 128-row tile, 16-bit
+constexpr int kBox = 128 * 128;             // 64 columns x 128 rows, 16-bit
+constexpr int kOffQ = 0;
+constexpr int kOffRing = 2 * kHalfBytes;
+constexpr int kOffBar = kOffRing + kStagesD * kHalfBytes;
+constexpr int kBarQ = 0;
+constexpr int kBarFull = 1;
+constexpr int kBarEmpty = kBarFull + kStagesD;
+constexpr int kBarS = kBarEmpty + kStagesD;   // [2] S_b ready
+constexpr int kBarP = kBarS + 2;              // [2] P in S_b (128 arrivals)
+constexpr int kBarPV = kBarP + 2;             // [2] P V of tile j done (barrier j & 1)
+constexpr int kBarDrain = kBarPV + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemD256 = kOffMisc + 16 + 1024;   // + alignment slack
+static_assert(kSmemD256 <= 232448, "fits the opt-in shared memory of one CTA");
+constexpr float kLn2f = 0.6931471805599453f;
+
+template <Elem E>
+struct LagD {
+  static constexpr float kTau = E == Elem::F16 ? 15.0f : 16.0f;
+};
+
+__device__ __forceinline__ int mini(int a, int b) { return a < b ? a : b; }
+
+// Query tile of unit u: head-major; causal tiles longest first within a head.
+__device__ __forceinline__ void tile_of(const D256Params& p, int u, int& bh, int& qt) {
+  bh = u / p.n_qt;
+  const int i = u - bh * p.n_qt;
+  qt = p.causal ? p.n_qt - 1 - i : i;
+}
+
+// Key tiles query tile qt needs: [0, n). Fully masked tiles are never loaded.
+__device__ __forceinline__ int key_tiles(const D256Params& p, int qt) {
+  if (!p.causal) return p.n_kv_tiles;
+  const int last_key = mini(qt * 128 + 127, p.N_q - 1) + p.kv_off;
+  return last_key < 0 ? 0 : mini(p.n_kv_tiles, last_key / 128 + 1);
+}
+
+__device__ __forceinline__ void drain_wait_d(uint32_t bar, uint32_t parity, int* status) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, &never, status);
+}
+
+template <Elem E>
+__global__ void __launch_bounds__(kThreads256, 1)
+    fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const D256Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int bh, qt;
+  tile_of(p, blockIdx.x, bh, qt);
+  const int n = key_tiles(p, qt);
+  const int b = bh / p.H_q;
+  const int bhk = b * p.H_kv + (bh - b * p.H_q) / (p.H_q / p.H_kv);
+  const int q0 = qt * 128;
+
+  if (warp == kWarpLoad && lane == 0) {
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < kStagesD; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarS + i), 1);
+      mbar_init(bar(kBarP + i), 128);
+      mbar_init(bar(kBarPV + i), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    // no global read or write before the previous kernel on the stream has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (n > 0) {
+      mbar_arrive_expect_tx(bar(kBarQ), 2 * kHalfBytes);
+#pragma unroll
+      for (int bx = 0; bx < 4; ++bx)
+        tma_load_3d(sb + kOffQ + bx * kBox, &tmQ, bar(kBarQ), bx * 64, q0, bh);
+    }
+  }
+  if (warp == kWarpIssue) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpLoad) {
+    // ======================= TMA producer =======================
+    // items in MMA order: K_0, K_1, then V_j, K_{j+2} for j = 0 .. n-1; each
+    // item is two d-halves, each one ring stage
+    if (lane == 0 && n > 0) {
+      const uint64_t pol = policy_evict_last();
+      int hs = 0;   // half-stages issued
+      bool ok = true;
+      auto load_item = [&](bool is_v, int j) {
+        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+          const int st = hs % kStagesD;
+          const uint32_t ph = (uint32_t)(hs / kStagesD) & 1u;
+          if (!mbar_wait(bar(kBarEmpty + st), ph ^ 1u, s_abort, p.status)) {
+            ok = false;
+            return;
+          }
+          mbar_arrive_expect_tx(bar(kBarFull + st), kHalfBytes);
+          const uint32_t dst = sb + kOffRing + st * kHalfBytes;
+          const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d_hint(dst + bx * kBox, map, bar(kBarFull + st), h * 128 + bx * 64, j * 128, bhk, pol);
+        }
+      };
+      load_item(false, 0);
+      if (n > 1) load_item(false, 1);
+      for (int j = 0; j < n && ok; ++j) {
+        load_item(true, j);
+        if (j + 2 < n) load_item(false, j + 2);
+      }
+      // every load issued has landed before the CTA may exit
+      drain_wait_d(bar(kBarQ), 0, p.status);
+      for (int st = 0; st < kStagesD; ++st) {
+        const int k = hs > st ? (hs - st + kStagesD - 1) / kStagesD : 0;
+        if (k > 0) drain_wait_d(bar(kBarFull + st), (uint32_t)(k - 1) & 1u, p.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpIssue) {
+    // ======================= tcgen05 MMA issuer =======================
+    if (n > 0) {
+      constexpr uint32_t idS = idesc_f32(128, 128, false, E);
+      constexpr uint32_t idO = idesc_f32(128, 128, true, E);
+      constexpr uint32_t kHi = desc_sw128_hi(1024);
+      const uint32_t lq = desc_sw128_lo(sb + kOffQ, 16);
+      const uint32_t lr = desc_sw128_lo(sb + kOffRing, 16);
+      const uint32_t lv = desc_sw128_lo(sb + kOffRing, kBox);
+      constexpr uint32_t kStageStep = (uint32_t)kHalfBytes >> 4;
+      constexpr uint32_t kBox16 = (uint32_t)kBox >> 4;
+      int hs = 0;   // half-stages consumed
+      bool ok = mbar_wait_w(bar(kBarQ), 0, s_abort, p.status);
+      // S(j) = Q K_j^T into S_(j&1): 16 MMAs of K = 16 over d, 8 per d-half stage
+      auto issue_S = [&](int j) {
+        const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
+        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+          const int st = hs % kStagesD;
+          if (!(ok = mbar_wait_w(bar(kBarFull + st), (uint32_t)(hs / kStagesD) & 1u, s_abort, p.status)))
+            return;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t offb = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+            const uint32_t offq = (uint32_t)(2 * h + (kk >> 2)) * kBox16 + (uint32_t)(kk & 3) * 2u;
+            mma_ss_lh_w(d, lq + offq, kHi, lr + (uint32_t)st * kStageStep + offb, kHi, idS,
+                        (h > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_w(bar(kBarEmpty + st));
+        }
+        if (ok) mma_commit_w(bar(kBarS + (j & 1)));
+      };
+      // O[:, 128h ..] (+)= P(j) V_j[:, 128h ..]: 8 MMAs of K = 16 keys per d-half
+      auto issue_PV = [&](int j) {
+        if (!(ok = mbar_wait_w(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, s_abort, p.status))) return;
+        tc_fence_after();
+        const uint32_t a = tmem + (uint32_t)(j & 1) * 128u;
+        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+          const int st = hs % kStagesD;
+          if (!(ok = mbar_wait_w(bar(kBarFull + st), (uint32_t)(hs / kStagesD) & 1u, s_abort, p.status)))
+            return;
+          tc_fence_after();
+          const uint32_t d = tmem + 256u + (uint32_t)h * 128u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_lh_w(d, a + (uint32_t)kk * 8u, lv + (uint32_t)st * kStageStep + (uint32_t)kk * (16u * 128u >> 4),
+                        kHi, idO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(bar(kBarEmpty + st));
+        }
+        if (ok) mma_commit_w(bar(kBarPV + (j & 1)));
+      };
+      if (ok) issue_S(0);
+      if (ok && n > 1) issue_S(1);
+      for (int j = 0; j < n && ok; ++j) {
+        issue_PV(j);
+        if (ok && j + 2 < n) issue_S(j + 2);
+      }
+      // all MMAs done before tensor memory is released
+      mma_commit_w(bar(kBarDrain));
+      drain_wait_d(bar(kBarDrain), 0, p.status);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ======================= softmax + epilogue =======================
+    const int r = warp * 32 + lane;       // row in the tile = TMEM lane
+    const int row = q0 + r;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_base + 256u;
+    const float c = p.c;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t tS = tmem + lane_base + (uint32_t)(j & 1) * 128u;
+      if (!(ok = mbar_wait(bar(kBarS + (j & 1)), (uint32_t)(j >> 1) & 1u, s_abort, p.status))) break;
+      tc_fence_after();
+      float s[128];
+      tmem_ld32(tS + 0, s);
+      tmem_ld32(tS + 32, s + 32);
+      tmem_ld32(tS + 64, s + 64);
+      tmem_ld32(tS + 96, s + 96);
+      tmem_wait_ld();
+      const int key0 = j * 128;
+      if (key0 + 128 > p.N_k || (p.causal && key0 + 127 > q0 + p.kv_off)) {
+        int lim = p.N_k - key0;
+        if (p.causal) lim = mini(lim, row + p.kv_off + 1 - key0);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) s[i] = -INFINITY;
+      }
+      float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; i += 4) {
+        a0 = max3f(a0, s[i], s[i + 1]);
+        a1 = max3f(a1, s[i + 2], s[i + 3]);
+      }
+      const float m_tile = fmaxf(a0, a1) * c;
+      // the reference is raised when the tile's max exceeds it by more than tau
+      // (always for a row's first live tile); O is rescaled once P V of the
+      // previous tile has completed
+      const bool need = m_tile > m_ref + LagD<E>::kTau;
+      if (__any_sync(0xffffffffu, need)) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_ref - m_tile);   // 0 when the row had no reference yet
+          m_ref = m_tile;
+          l *= alpha;
+        }
+        if (j > 0) {
+          if (!(ok = mbar_wait(bar(kBarPV + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, s_abort, p.status)))
+            break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < 256; cc += 32) {
+            float ov[32];
+            tmem_ld32(tO + cc, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            tmem_st32(tO + cc, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+      const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+      // P = 2^(s c - m_ref), packed two per column over the first 64 columns of S
+      float2 sa = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float pv[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 e = ffma2_bc(make_float2(s[16 * k + i], s[16 * k + i + 1]), c, -mb);
+          pv[i] = ex2_approx(e.x);
+          pv[i + 1] = ex2_approx(e.y);
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pk[i] = pack2<E>(pv[2 * i], pv[2 * i + 1]);
+        tmem_st8(tS + (uint32_t)k * 8u, pk);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          sa = fadd2(sa, make_float2(pv[i], pv[i + 1]));
+          sb2 = fadd2(sb2, make_float2(pv[i + 2], pv[i + 3]));
+        }
+      }
+      l += (sa.x + sa.y) + (sb2.x + sb2.y);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kBarP + (j & 1)));
+    }
+    if (ok && n > 0) {
+      ok = mbar_wait(bar(kBarPV + ((n - 1) & 1)), (uint32_t)((n - 1) >> 1) & 1u, s_abort, p.status);
+      tc_fence_after();
+    }
+    // O / l -> 16-bit, staged in the Q tile's (now idle) 64-column swizzled
+    // boxes, one TMA store of four boxes; LSE direct
+    const uint32_t obase = sb + kOffQ;
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < kD; cc += 32) {
+        float ov[32];
+        if (n > 0) {
+          tmem_ld32(tO + cc, ov);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
+        const uint32_t rowaddr = obase + (uint32_t)(cc >> 6) * kBox + (uint32_t)r * 128u;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t ch = (uint32_t)(((cc & 63) >> 3) + g);
+          st_shared_v4(rowaddr + ((ch ^ (uint32_t)(r & 7)) << 4),
+                       pack2<E>(ov[8 * g + 0] * inv, ov[8 * g + 1] * inv),
+                       pack2<E>(ov[8 * g + 2] * inv, ov[8 * g + 3] * inv),
+                       pack2<E>(ov[8 * g + 4] * inv, ov[8 * g + 5] * inv),
+                       pack2<E>(ov[8 * g + 6] * inv, ov[8 * g + 7] * inv));
+        }
+      }
+      if (row < p.N_q && p.lse)
+        p.lse[(size_t)bh * p.N_q + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2f : -INFINITY;
+    }
+    fence_proxy_async_smem();
+    const bool all_ok = named_bar_and(1, 128, ok);
+    if (all_ok && r == 0) {   // rows past N_q are clipped by the TMA
+#pragma unroll
+      for (int bx = 0; bx < 4; ++bx) tma_store_3d(&tmO, obase + bx * kBox, bx * 64, q0, bh);
+      bulk_commit();
+      bulk_wait_read0();
+    }
+  }
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpIssue) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <Elem E>
+cudaError_t launch_d256_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream) {
+  static bool attr[64] = {false};   // benign race: setting the attribute twice is harmless
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_d256_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemD256);
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)units);
+  cfg.blockDim = dim3(kThreads256);
+  cfg.dynamicSmemBytes = kSmemD256;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_fwd_d256_kernel<E>, tq, tk, tv, to, p);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream) {
+  if (units <= 0) return cudaSuccess;
+  return p.elem == (int)Elem::F16 ? launch_d256_t<Elem::F16>(tq, tk, tv, to, p, units, stream)
+                                  : launch_d256_t<Elem::BF16>(tq, tk, tv, to, p, units, stream);
+}
+
+}  // namespace fa

@@ -68,6 +68,22 @@ cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, c
 typedef cudaError_t (*PairedLaunch)(int d, const FwdMaps& m, const FwdParams& p, int units,
                                     cudaStream_t stream);
 
+// ---- fused forward for head dimension 256 (one 128-row query tile per CTA) -----------
+struct D256Params {
+  int B, H_q, H_kv, N_q, N_k;
+  int causal;
+  int kv_off;       // N_k - N_q
+  int n_qt;         // ceil(N_q / 128) query tiles per (b, h)
+  int n_kv_tiles;   // ceil(N_k / 128)
+  int elem;         // 0 = BF16, 1 = FP16
+  float c;          // scale * log2(e)
+  float* lse;       // fp32 [B][H_q][N_q] or nullptr
+  int* status;
+};
+// One CTA per query tile (B * H_q * n_qt CTAs), as a programmatic dependent launch.
+cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream);
+
 // ---- decode / few queries per KV head -------------------------------------------------
 constexpr int kDecodeMaxRows = 16;   // R = G * N_q rows per KV head must fit one m16 MMA
 

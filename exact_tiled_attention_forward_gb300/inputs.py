@@ -339,6 +339,9 @@ WORKLOADS = {
                                          causal=True, k_row_frac=0.01),
     "decode_b16_h32_kv8_n8192_d128": dict(B=16, H_q=32, H_kv=8, N_q=1, N_k=8192, d=128,
                                           causal=False),
+    # head dimension 256 (the forward's widest tile plan)
+    "h32_n4096_d256": dict(B=1, H_q=32, H_kv=32, N_q=4096, N_k=4096, d=256, causal=False),
+    "h32_n4096_d256_causal": dict(B=1, H_q=32, H_kv=32, N_q=4096, N_k=4096, d=256, causal=True),
 }
 
 

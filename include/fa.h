@@ -36,7 +36,9 @@
  *    key gets O = 0 and LSE = -inf.
  *  - lse[i] = ln(sum_j exp(scale * q_i . k_j)) over the visible keys.
  *  - scale must be finite and > 0 (1/sqrt(d) is the usual value).
- *  - d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise; 128 for FP8 inputs).
+ *  - d must be 64 or 128, or 256 for the forward entry points fa_forward,
+ *    fa_forward_fp16, fa_forward_noalloc and fa_forward_host[_packed]
+ *    (FA_ERR_UNSUPPORTED otherwise; FP8 inputs: 128).
  *  - stream: a cudaStream_t (NULL = legacy default stream). Calls are
  *    asynchronous: they return once the work is enqueued. Argument errors are
  *    reported before anything is enqueued. Launch errors return FA_ERR_CUDA
@@ -57,7 +59,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = -1, /* null/misaligned/overlapping pointer, bad size, H_q % H_kv, scale */
-  FA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (d not 64/128) */
+  FA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (head dim, entry point) */
   FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   FA_ERR_NO_MEMORY = -4,   /* stream-ordered workspace allocation failed, or workspace too small */
   FA_ERR_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (device status word) */
@@ -81,6 +83,9 @@ typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 } fa_dtype;
  * Decode / few queries (the H_q/H_kv * N_q query rows that share a KV head
  * number at most 16): one CTA per (batch, KV head, 128-key chunk) reads its
  * K and V chunk once for all those rows; chunk partials are merged the same way.
+ * Head dimension 256: one CTA per 128-row query tile (a 256-column output tile
+ * fills half of the SM's tensor memory), two 128-key score buffers in turn,
+ * K and V in 128-column halves; no key-range split, no workspace, one launch.
  * Split and decode partials live in a stream-ordered workspace taken from a
  * library-owned memory pool on the current device (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`); the pool keeps freed memory reserved for later
@@ -169,7 +174,8 @@ int fa_forward_host_packed(int n, const void* const* qkv, void* const* out, int 
  * workspace from libfa's pool. Deterministic (no atomics). Pointers: device, 16-byte aligned; the
  * outputs may not overlap any input or each other. When N_q or N_k is 0 the
  * gradients that exist are zero-filled. Returns FA_OK, FA_ERR_INVALID_ARG,
- * FA_ERR_UNSUPPORTED (d not 64/128), FA_ERR_NO_MEMORY or FA_ERR_CUDA. */
+ * FA_ERR_UNSUPPORTED (d not 64/128; d = 256 is forward-only), FA_ERR_NO_MEMORY
+ * or FA_ERR_CUDA. */
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N_q,
                 int N_k, int d, int causal, float scale, int dtype, void* stream);

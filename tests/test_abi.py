@@ -105,7 +105,7 @@ def _fwd(lib, q=Q, k=K, v=V, o=O, l=L, B=1, Hq=2, Hkv=1, Nq=64, Nk=64, d=128, ca
     (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
     (dict(d=0), fa.FA_ERR_INVALID_ARG),
     (dict(q=0), fa.FA_ERR_INVALID_ARG),                    # null q
     (dict(o=0), fa.FA_ERR_INVALID_ARG),
@@ -127,6 +127,21 @@ def test_noalloc_rejects_like_forward(lib):
     assert f(Q, K, V, O, L, 1, 2, 1, 64, 64, 96, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
     assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
     assert f(0, 0, 0, 0, 0, 1, 2, 1, 0, 64, 128, 0, 0.1, None) == fa.FA_OK
+
+
+def test_head_dim_256_only_on_the_forward(lib):
+    # d = 256 is a forward-only head dimension: the backward, the paged decode and
+    # the unfused baseline refuse it before anything else runs
+    need = lib.fa_naive_workspace_bytes(1, 2, 64, 64)
+    assert lib.fa_naive_forward(Q, K, V, O, L, 1, 2, 1, 64, 64, 256, 0, 0.1, 0x60000000, need,
+                                None) == fa.FA_ERR_UNSUPPORTED
+    D1, D2, D3 = 0x70000000, 0x80000000, 0x90000000
+    assert lib.fa_backward(Q, K, V, O, L, O, D1, D2, D3, 1, 2, 1, 64, 64, 256, 0, 0.1, 0,
+                           None) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_decode_paged(Q, K, V, D1, D2, O, L, 1, 2, 1, 1, 4, 2, 256, 0, 0.1, 0,
+                               None) == fa.FA_ERR_UNSUPPORTED
+    plan = fa.fa_forward_plan(2, 4, 2, 300, 500, 256, True)
+    assert plan == {"ctas": 2 * 4 * 3, "launches": 1, "workspace_bytes": 0}
 
 
 def test_fp8_rejects(lib):
