@@ -407,7 +407,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     if (!make_tmap_bf16_3d(&tq, q, d, N_q, (uint64_t)B * H_q, d, 128) ||
         !make_tmap_bf16_3d(&to, o, d, N_q, (uint64_t)B * H_q, d, 128))
       return cuda_fail(cudaErrorInvalidValue);
-    cudaError_t e = launch_fwd_d256(tq, tk, tv, to, p, (int)units, strm);
+    cudaError_t e = launch_fwd_tile(d, tq, tk, tv, to, p, (int)units, strm);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
   }
 

@@ -1,4 +1,5 @@
-// Fused exact attention forward for head dimension 256 (BF16 or FP16 tensors).
+// Fused exact attention forward for head dimension 256 (BF16 or FP16 tensors):
+// one query tile per CTA ("tile kernel").
 //
 // Same method as the d = 64 / 128 kernel ("Flash Attention Mechanics", "The
 // Tiling Algorithm"; "Why is standard attention memory-bound...", Step 3): a
@@ -37,28 +38,40 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 256;
 constexpr int kThreads256 = 256;
 constexpr int kWarpLoad = 4;
 constexpr int kWarpIssue = 5;
-constexpr int kStagesD = 5;
-constexpr int kHalfBytes = 128 * 128 * 2;   // one d-half of a 128-row tile, 16-bit
+constexpr int kHalfBytes = 128 * 128 * 2;   // 128 rows x 128 columns (a "half" of d = 256), 16-bit
 constexpr int kBox = 128 * 128;             // 64 columns x 128 rows, 16-bit
-constexpr int kOffQ = 0;
-constexpr int kOffRing = 2 * kHalfBytes;
-constexpr int kOffBar = kOffRing + kStagesD * kHalfBytes;
-constexpr int kBarQ = 0;
-constexpr int kBarFull = 1;
-constexpr int kBarEmpty = kBarFull + kStagesD;
-constexpr int kBarS = kBarEmpty + kStagesD;   // [2] S_b ready
-constexpr int kBarP = kBarS + 2;              // [2] P in S_b (128 arrivals)
-constexpr int kBarPV = kBarP + 2;             // [2] P V of tile j done (barrier j & 1)
-constexpr int kBarDrain = kBarPV + 2;
-constexpr int kNumBars = kBarDrain + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemD256 = kOffMisc + 16 + 1024;   // + alignment slack
-static_assert(kSmemD256 <= 232448, "fits the opt-in shared memory of one CTA");
 constexpr float kLn2f = 0.6931471805599453f;
+
+// Layout for head dimension D (128 or 256). A K or V tile of D columns takes
+// D / 128 ring stages of 32 KB. S buffers: three at D = 128 (3 x 128 + 128 TMEM
+// columns), two at D = 256 (2 x 128 + 256): enough that the tensor core has the
+// next tiles' products queued while the softmax works on one.
+template <int D>
+struct TileCfg {
+  static constexpr int kHalves = D / 128;
+  static constexpr int kNS = D == 256 ? 2 : 3;
+  static constexpr uint32_t kTmO = 128u * kNS;
+  static constexpr int kStages = D == 256 ? 5 : 6;
+  static constexpr int kQBytes = 128 * D * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = kQBytes;
+  static constexpr int kOffBar = kOffRing + kStages * kHalfBytes;
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = kBarFull + kStages;
+  static constexpr int kBarS = kBarEmpty + kStages;   // [kNS] S_b ready
+  static constexpr int kBarP = kBarS + kNS;           // [kNS] P in S_b (128 arrivals)
+  static constexpr int kBarPV = kBarP + kNS;          // [4] P V of tile j done (barrier j & 3)
+  static constexpr int kBarDrain = kBarPV + 4;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffMisc + 16 + 1024;   // + alignment slack
+  static_assert(kSmem <= 232448, "fits the opt-in shared memory of one CTA");
+  static_assert(kTmO + D <= 512, "S buffers and O fit the 512 TMEM columns");
+};
 
 template <Elem E>
 struct LagD {
@@ -86,11 +99,17 @@ __device__ __forceinline__ void drain_wait_d(uint32_t bar, uint32_t parity, int*
   mbar_wait(bar, parity, &never, status);
 }
 
-template <Elem E>
+template <int D, Elem E>
 __global__ void __launch_bounds__(kThreads256, 1)
-    fa_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    fa_fwd_tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        const D256Params p) {
+  using T = TileCfg<D>;
+  constexpr int kStagesD = T::kStages;
+  constexpr int kOffQ = T::kOffQ, kOffRing = T::kOffRing, kOffBar = T::kOffBar, kOffMisc = T::kOffMisc;
+  constexpr int kBarQ = T::kBarQ, kBarFull = T::kBarFull, kBarEmpty = T::kBarEmpty, kBarS = T::kBarS;
+  constexpr int kBarP = T::kBarP, kBarPV = T::kBarPV, kBarDrain = T::kBarDrain;
+  constexpr int kNS = T::kNS, kHalves = T::kHalves;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -114,11 +133,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(kBarS + i), 1);
       mbar_init(bar(kBarP + i), 128);
-      mbar_init(bar(kBarPV + i), 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarPV + i), 1);
     mbar_init(bar(kBarDrain), 1);
     *s_abort = 0;
     fence_mbar_init();
@@ -130,9 +149,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
     // no global read or write before the previous kernel on the stream has finished
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (n > 0) {
-      mbar_arrive_expect_tx(bar(kBarQ), 2 * kHalfBytes);
+      mbar_arrive_expect_tx(bar(kBarQ), T::kQBytes);
 #pragma unroll
-      for (int bx = 0; bx < 4; ++bx)
+      for (int bx = 0; bx < D / 64; ++bx)
         tma_load_3d(sb + kOffQ + bx * kBox, &tmQ, bar(kBarQ), bx * 64, q0, bh);
     }
   }
@@ -147,14 +166,14 @@ __global__ void __launch_bounds__(kThreads256, 1)
 
   if (warp == kWarpLoad) {
     // ======================= TMA producer =======================
-    // items in MMA order: K_0, K_1, then V_j, K_{j+2} for j = 0 .. n-1; each
-    // item is two d-halves, each one ring stage
+    // items in MMA order: K_0 .. K_{kNS-1}, then V_j, K_{j+kNS} for j = 0 .. n-1;
+    // each item is D / 128 ring stages (128 columns each)
     if (lane == 0 && n > 0) {
       const uint64_t pol = policy_evict_last();
       int hs = 0;   // half-stages issued
       bool ok = true;
       auto load_item = [&](bool is_v, int j) {
-        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+        for (int h = 0; h < kHalves && ok; ++h, ++hs) {
           const int st = hs % kStagesD;
           const uint32_t ph = (uint32_t)(hs / kStagesD) & 1u;
           if (!mbar_wait(bar(kBarEmpty + st), ph ^ 1u, s_abort, p.status)) {
@@ -169,11 +188,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
             tma_load_3d_hint(dst + bx * kBox, map, bar(kBarFull + st), h * 128 + bx * 64, j * 128, bhk, pol);
         }
       };
-      load_item(false, 0);
-      if (n > 1) load_item(false, 1);
+      for (int j = 0; j < kNS && j < n && ok; ++j) load_item(false, j);
       for (int j = 0; j < n && ok; ++j) {
         load_item(true, j);
-        if (j + 2 < n) load_item(false, j + 2);
+        if (j + kNS < n) load_item(false, j + kNS);
       }
       // every load issued has landed before the CTA may exit
       drain_wait_d(bar(kBarQ), 0, p.status);
@@ -196,10 +214,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
       constexpr uint32_t kBox16 = (uint32_t)kBox >> 4;
       int hs = 0;   // half-stages consumed
       bool ok = mbar_wait_w(bar(kBarQ), 0, s_abort, p.status);
-      // S(j) = Q K_j^T into S_(j&1): 16 MMAs of K = 16 over d, 8 per d-half stage
+      // S(j) = Q K_j^T into S_(j % kNS): D / 16 MMAs of K = 16, 8 per 128-column stage
       auto issue_S = [&](int j) {
-        const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
-        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+        const uint32_t d = tmem + (uint32_t)(j % kNS) * 128u;
+        for (int h = 0; h < kHalves && ok; ++h, ++hs) {
           const int st = hs % kStagesD;
           if (!(ok = mbar_wait_w(bar(kBarFull + st), (uint32_t)(hs / kStagesD) & 1u, s_abort, p.status)))
             return;
@@ -213,32 +231,31 @@ __global__ void __launch_bounds__(kThreads256, 1)
           }
           mma_commit_w(bar(kBarEmpty + st));
         }
-        if (ok) mma_commit_w(bar(kBarS + (j & 1)));
+        if (ok) mma_commit_w(bar(kBarS + j % kNS));
       };
       // O[:, 128h ..] (+)= P(j) V_j[:, 128h ..]: 8 MMAs of K = 16 keys per d-half
       auto issue_PV = [&](int j) {
-        if (!(ok = mbar_wait_w(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, s_abort, p.status))) return;
+        if (!(ok = mbar_wait_w(bar(kBarP + j % kNS), (uint32_t)(j / kNS) & 1u, s_abort, p.status))) return;
         tc_fence_after();
-        const uint32_t a = tmem + (uint32_t)(j & 1) * 128u;
-        for (int h = 0; h < 2 && ok; ++h, ++hs) {
+        const uint32_t a = tmem + (uint32_t)(j % kNS) * 128u;
+        for (int h = 0; h < kHalves && ok; ++h, ++hs) {
           const int st = hs % kStagesD;
           if (!(ok = mbar_wait_w(bar(kBarFull + st), (uint32_t)(hs / kStagesD) & 1u, s_abort, p.status)))
             return;
           tc_fence_after();
-          const uint32_t d = tmem + 256u + (uint32_t)h * 128u;
+          const uint32_t d = tmem + T::kTmO + (uint32_t)h * 128u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts_lh_w(d, a + (uint32_t)kk * 8u, lv + (uint32_t)st * kStageStep + (uint32_t)kk * (16u * 128u >> 4),
                         kHi, idO, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(bar(kBarEmpty + st));
         }
-        if (ok) mma_commit_w(bar(kBarPV + (j & 1)));
+        if (ok) mma_commit_w(bar(kBarPV + (j & 3)));
       };
-      if (ok) issue_S(0);
-      if (ok && n > 1) issue_S(1);
+      for (int j = 0; j < kNS && j < n && ok; ++j) issue_S(j);
       for (int j = 0; j < n && ok; ++j) {
         issue_PV(j);
-        if (ok && j + 2 < n) issue_S(j + 2);
+        if (ok && j + kNS < n) issue_S(j + kNS);
       }
       // all MMAs done before tensor memory is released
       mma_commit_w(bar(kBarDrain));
@@ -250,14 +267,14 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const int r = warp * 32 + lane;       // row in the tile = TMEM lane
     const int row = q0 + r;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_base + 256u;
+    const uint32_t tO = tmem + lane_base + T::kTmO;
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
-      const uint32_t tS = tmem + lane_base + (uint32_t)(j & 1) * 128u;
-      if (!(ok = mbar_wait(bar(kBarS + (j & 1)), (uint32_t)(j >> 1) & 1u, s_abort, p.status))) break;
+      const uint32_t tS = tmem + lane_base + (uint32_t)(j % kNS) * 128u;
+      if (!(ok = mbar_wait(bar(kBarS + j % kNS), (uint32_t)(j / kNS) & 1u, s_abort, p.status))) break;
       tc_fence_after();
       float s[128];
       tmem_ld32(tS + 0, s);
@@ -292,11 +309,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
           l *= alpha;
         }
         if (j > 0) {
-          if (!(ok = mbar_wait(bar(kBarPV + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, s_abort, p.status)))
+          if (!(ok = mbar_wait(bar(kBarPV + ((j - 1) & 3)), (uint32_t)((j - 1) >> 2) & 1u, s_abort, p.status)))
             break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 256; cc += 32) {
+          for (int cc = 0; cc < D; cc += 32) {
             float ov[32];
             tmem_ld32(tO + cc, ov);
             tmem_wait_ld();
@@ -332,10 +349,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
       l += (sa.x + sa.y) + (sb2.x + sb2.y);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kBarP + (j & 1)));
+      mbar_arrive(bar(kBarP + j % kNS));
     }
     if (ok && n > 0) {
-      ok = mbar_wait(bar(kBarPV + ((n - 1) & 1)), (uint32_t)((n - 1) >> 1) & 1u, s_abort, p.status);
+      ok = mbar_wait(bar(kBarPV + ((n - 1) & 3)), (uint32_t)((n - 1) >> 2) & 1u, s_abort, p.status);
       tc_fence_after();
     }
     // O / l -> 16-bit, staged in the Q tile's (now idle) 64-column swizzled
@@ -344,7 +361,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < kD; cc += 32) {
+      for (int cc = 0; cc < D; cc += 32) {
         float ov[32];
         if (n > 0) {
           tmem_ld32(tO + cc, ov);
@@ -371,7 +388,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const bool all_ok = named_bar_and(1, 128, ok);
     if (all_ok && r == 0) {   // rows past N_q are clipped by the TMA
 #pragma unroll
-      for (int bx = 0; bx < 4; ++bx) tma_store_3d(&tmO, obase + bx * kBox, bx * 64, q0, bh);
+      for (int bx = 0; bx < D / 64; ++bx) tma_store_3d(&tmO, obase + bx * kBox, bx * 64, q0, bh);
       bulk_commit();
       bulk_wait_read0();
     }
@@ -385,38 +402,42 @@ __global__ void __launch_bounds__(kThreads256, 1)
   }
 }
 
-template <Elem E>
-cudaError_t launch_d256_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, Elem E>
+cudaError_t launch_tile_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream) {
   static bool attr[64] = {false};   // benign race: setting the attribute twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_d256_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemD256);
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_tile_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TileCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)units);
   cfg.blockDim = dim3(kThreads256);
-  cfg.dynamicSmemBytes = kSmemD256;
+  cfg.dynamicSmemBytes = TileCfg<D>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_d256_kernel<E>, tq, tk, tv, to, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_tile_kernel<D, E>, tq, tk, tv, to, p);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+// (The same layout fits D = 128 with three score buffers; measured on GB300 it
+// ran no faster than the two-tile kernel there at 32 heads x 4096 and slower on
+// one head, so d = 128 keeps the two-tile kernel and only d = 256 comes here.)
+cudaError_t launch_fwd_tile(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
-  return p.elem == (int)Elem::F16 ? launch_d256_t<Elem::F16>(tq, tk, tv, to, p, units, stream)
-                                  : launch_d256_t<Elem::BF16>(tq, tk, tv, to, p, units, stream);
+  if (d != 256) return cudaErrorInvalidValue;
+  return p.elem == (int)Elem::F16 ? launch_tile_t<256, Elem::F16>(tq, tk, tv, to, p, units, stream)
+                                  : launch_tile_t<256, Elem::BF16>(tq, tk, tv, to, p, units, stream);
 }
 
 }  // namespace fa

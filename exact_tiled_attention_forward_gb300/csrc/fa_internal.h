@@ -80,8 +80,9 @@ struct D256Params {
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
   int* status;
 };
-// One CTA per query tile (B * H_q * n_qt CTAs), as a programmatic dependent launch.
-cudaError_t launch_fwd_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+// One CTA per query tile (B * H_q * n_qt CTAs), as a programmatic dependent
+// launch; head dimension d = 128 or 256.
+cudaError_t launch_fwd_tile(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const D256Params& p, int units, cudaStream_t stream);
 
 // ---- decode / few queries per KV head -------------------------------------------------
