@@ -33,6 +33,7 @@ FA_ERR_CUDA = -3
 FA_ERR_NO_MEMORY = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
+FA_ERR_BOUNDS = -7
 
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP16 = 1
@@ -69,6 +70,8 @@ _SIGNATURES = {
     "fa_forward_plan": (_c_int, [_c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong),
                                                 ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
     "fa_selftest_wait_timeout": (_c_int, [ctypes.c_ulonglong, _vp]),
+    "fa_selftest_bounds": (_c_int, [_vp]),
+    "fa_debug_build": (_c_int, []),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_get_last_cuda_error": (_c_int, []),
     "fa_device_status": (_c_int, [_c_int]),

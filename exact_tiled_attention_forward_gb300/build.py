@@ -24,6 +24,11 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 LIB_SINGLE_GPU = os.path.join(BUILD, "libfa_single_gpu.so")
+# FA_DEBUG build of libfa (device-side bounds checks that report instead of
+# touching memory out of range): a separate library, never the one the
+# binding loads by default
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libfa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -40,26 +45,30 @@ def sources(folder=CSRC):
     return sorted(os.path.join(folder, f) for f in os.listdir(folder) if f.endswith(".cu"))
 
 
-def _stale() -> bool:
-    if not (os.path.exists(LIB) and os.path.exists(LIB_SINGLE_GPU)):
+def _stale(outputs=(LIB, LIB_SINGLE_GPU)) -> bool:
+    if not all(os.path.exists(o) for o in outputs):
         return True
-    t = min(os.path.getmtime(LIB), os.path.getmtime(LIB_SINGLE_GPU))
+    t = min(os.path.getmtime(o) for o in outputs)
     deps = sources() + sources(CSRC_SINGLE)
     for folder in (CSRC, CSRC_SINGLE, INCLUDE):
         deps += [os.path.join(folder, f) for f in os.listdir(folder) if f.endswith((".cuh", ".h"))]
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link both libraries if any source is newer than them; return libfa.so's path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link both libraries if any source is newer than them; return
+    libfa.so's path. debug=True builds only the FA_DEBUG libfa (_build_debug/)."""
+    out_dir = BUILD_DEBUG if debug else BUILD
+    outputs = (LIB_DEBUG,) if debug else (LIB, LIB_SINGLE_GPU)
+    if not force and not _stale(outputs):
+        return outputs[0]
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
+    flags = [*FLAGS, *extra_flags] + (["-DFA_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -67,19 +76,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    base, single = sources(), sources(CSRC_SINGLE)
+    base, single = sources(), ([] if debug else sources(CSRC_SINGLE))
     with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
         objs = list(ex.map(compile_one, base + single))
     base_objs, single_objs = objs[:len(base)], objs[len(base):]
-    for out, parts in ((LIB, base_objs), (LIB_SINGLE_GPU, base_objs + single_objs)):
+    links = ((LIB_DEBUG, base_objs),) if debug else ((LIB, base_objs), (LIB_SINGLE_GPU, base_objs + single_objs))
+    for out, parts in links:
         tmp = out + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *parts]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link of {os.path.basename(out)} failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, out)
-    return LIB
+    return outputs[0]
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -1,6 +1,7 @@
 // C ABI of libfa: argument validation, tensor-map construction, work split
 // and launches. Declared in include/fa.h.
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 #include "fa.h"
 
 #include <cuda_bf16.h>
@@ -521,6 +522,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_NO_MEMORY: return "out of memory / workspace too small";
     case FA_ERR_TIMEOUT: return "kernel wait timed out";
     case FA_ERR_TOO_LARGE: return "request needs more scratch than the static scratch array holds";
+    case FA_ERR_BOUNDS: return "a bounds check of the FA_DEBUG build failed";
     default: return "unknown status";
   }
 }
@@ -540,7 +542,7 @@ int fa_device_status(int reset) {
     e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  return h == 0 ? FA_OK : FA_ERR_TIMEOUT;
+  return h == 0 ? FA_OK : (h == FA_DEV_BOUNDS ? FA_ERR_BOUNDS : FA_ERR_TIMEOUT);
 }
 
 int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal, long long* ctas,

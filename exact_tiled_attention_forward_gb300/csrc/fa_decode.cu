@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kDecThreads)
         cml[2 * m] = L > 0.f ? M : -INFINITY;
         cml[2 * m + 1] = L;
       }
-    } else {
+    } else if (FA_DBG_OK(p.status, (size_t)pbase + m < (size_t)p.B * p.H_kv * p.n_parts * p.R && dcol < D)) {
       __stcg(p.part_o + (pbase + m) * D + dcol, acc);
       if (dcol == 0)
         __stcg(reinterpret_cast<float2*>(p.part_ml) + pbase + m, make_float2(L > 0.f ? M : -INFINITY, L));
@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(kDecThreads)
       const int hl = m / p.N_q, i = m - hl * p.N_q;
       const int hq = hk * p.G + hl;
       const size_t orow = ((size_t)b * p.H_q + hq) * p.N_q + i;
+      if (!FA_DBG_OK(p.status, orow < (size_t)p.B * p.H_q * p.N_q && dcol + 4 <= D)) continue;
       uint2 o2;
       o2.x = pack2<E>(acc.x, acc.y);
       o2.y = pack2<E>(acc.z, acc.w);

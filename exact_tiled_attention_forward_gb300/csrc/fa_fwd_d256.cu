@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // FA_DEBUG bounds: the usable shared memory is [sb, s_hi)
+  [[maybe_unused]] const uint32_t s_hi = sb + (uint32_t)(T::kSmem - 1024);
 
   int bh, qt;
   tile_of(p, blockIdx.x, bh, qt);
@@ -183,6 +185,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
           mbar_arrive_expect_tx(bar(kBarFull + st), kHalfBytes);
           const uint32_t dst = sb + kOffRing + st * kHalfBytes;
           const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
+          if (!FA_DBG_OK(p.status, smem_in(dst, kHalfBytes, sb + kOffRing, sb + kOffBar) && j < p.n_kv_tiles))
+            continue;   // FA_DEBUG: reported, not loaded
 #pragma unroll
           for (int bx = 0; bx < 2; ++bx)
             tma_load_3d_hint(dst + bx * kBox, map, bar(kBarFull + st), h * 128 + bx * 64, j * 128, bhk, pol);
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       bool ok = mbar_wait_w(bar(kBarQ), 0, s_abort, p.status);
       // S(j) = Q K_j^T into S_(j % kNS): D / 16 MMAs of K = 16, 8 per 128-column stage
       auto issue_S = [&](int j) {
+        if (!FA_DBG_OK(p.status, tmem_in((uint32_t)(j % kNS) * 128u, 128, T::kTmO))) return;
         const uint32_t d = tmem + (uint32_t)(j % kNS) * 128u;
         for (int h = 0; h < kHalves && ok; ++h, ++hs) {
           const int st = hs % kStagesD;
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       auto issue_PV = [&](int j) {
         if (!(ok = mbar_wait_w(bar(kBarP + j % kNS), (uint32_t)(j / kNS) & 1u, s_abort, p.status))) return;
         tc_fence_after();
+        if (!FA_DBG_OK(p.status, tmem_in(T::kTmO, D))) return;
         const uint32_t a = tmem + (uint32_t)(j % kNS) * 128u;
         for (int h = 0; h < kHalves && ok; ++h, ++hs) {
           const int st = hs % kStagesD;
@@ -277,6 +283,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (!(ok = mbar_wait(bar(kBarS + j % kNS), (uint32_t)(j / kNS) & 1u, s_abort, p.status))) break;
       tc_fence_after();
       float s[128];
+      if (!FA_DBG_OK(p.status, tmem_in(lane_base + (uint32_t)(j % kNS) * 128u, 128, T::kTmO) &&
+                                   tmem_in(lane_base + T::kTmO, D))) {
+        ok = false;   // FA_DEBUG: reported; this tile is not processed
+        break;
+      }
       tmem_ld32(tS + 0, s);
       tmem_ld32(tS + 32, s + 32);
       tmem_ld32(tS + 64, s + 64);
@@ -358,6 +369,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     // O / l -> 16-bit, staged in the Q tile's (now idle) 64-column swizzled
     // boxes, one TMA store of four boxes; LSE direct
     const uint32_t obase = sb + kOffQ;
+    if (ok && !FA_DBG_OK(p.status, smem_in(obase, D / 64 * kBox, sb, s_hi) && bh < p.B * p.H_q))
+      ok = false;   // FA_DEBUG: reported; nothing stored
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1

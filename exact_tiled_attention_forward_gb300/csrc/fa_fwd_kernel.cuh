@@ -432,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // FA_DEBUG bounds: the usable shared memory is [sb, s_hi)
+  [[maybe_unused]] const uint32_t s_hi = sb + (uint32_t)(C::kSmemBytes - 1024);
 
   // barriers first (the plain kernel's counts do not depend on the unit), so
   // their set-up overlaps the parameter loads of the unit decode below
@@ -559,7 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(C::kBarFull + st), C::kTileBytes);
             const void* tmap = sel ? (const void*)&tmV : (const void*)&tmK;
             const uint32_t dst = sb + C::kOffKV + st * C::kTileBytes;
-            if (!MC) {
+            if (!FA_DBG_OK(p.status, smem_in(dst, C::kTileBytes, sb + C::kOffKV, sb + C::kOffBar) &&
+                                         tile < p.n_kv_tiles)) {
+              // FA_DEBUG: reported, not loaded (the consumer's bounded wait then gives up)
+            } else if (!MC) {
 #pragma unroll
               for (int bx = 0; bx < C::kBoxes; ++bx)
                 tma_load_3d_hint(dst + bx * C::kBoxBytes, tmap, bar(C::kBarFull + st), bx * C::kBoxCols,
@@ -619,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lv0 = desc_sw128_lo(sb + C::kOffKV, C::kBoxBytes);
         // MMA kk of S covers bytes 32kk .. 32kk+31 of each 128-byte box row
         auto issue_S = [&](int X, int st) {
+          if (!FA_DBG_OK(p.status, st < C::kStages && tmem_in(C::tm_s(X), 128))) return;
           const uint32_t a0 = lq0 + (uint32_t)X * kStageStep;
           const uint32_t b0 = lk0 + (uint32_t)st * kStageStep;
           const uint32_t d = tmem + C::tm_s(X);
@@ -637,6 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_PV = [&](int X, int st, bool acc, int h) {   // keys 64h .. 64h+63
           constexpr int kPer = 64 / C::kPVKeys;
           constexpr uint32_t kVStep = (uint32_t)(C::kPVKeys * 128) >> 4;
+          if (!FA_DBG_OK(p.status, st < C::kStages && tmem_in(C::tm_o(X), D) &&
+                                       tmem_in(C::tm_s(X), 2 * C::kPHalfCols)))
+            return;
           const uint32_t b0 = lv0 + (uint32_t)st * kStageStep;
           const uint32_t d = tmem + C::tm_o(X);
           const uint32_t a = tmem + C::tm_s(X);
@@ -726,6 +735,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(bar(C::kBarS + X), (uint32_t)j & 1u, s_abort, p.status))) break;
       tc_fence_after();
       float s[kTileN];
+      if (!FA_DBG_OK(p.status, tmem_in(lane_base + C::tm_s(X), kTileN) &&
+                                   tmem_in(lane_base + C::tm_o(X), D))) {
+        ok = false;   // FA_DEBUG: reported; this tile is not processed
+        break;
+      }
       tmem_ld32(tS + 0, s);
       tmem_ld32(tS + 32, s + 32);
       tmem_ld32(tS + 64, s + 64);
@@ -797,7 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // threads pass the first cluster barrier: the Q tiles and the K/V ring
       // are free and receive the partials (warpgroup 2 takes the same barriers)
       cluster_sync();
-      cm_send<D>(sb + C::kOffQ, sb + C::kOffCm, p.s_tail, ui.split, X * kTileM + r, tO, n, m_ref, l);
+      // FA_DEBUG: the receive slots ([sender][16-byte chunk][row], S senders x
+      // 256 / S rows each) span exactly [0, kCmStage) for S in {2, 4, 8}
+      if (FA_DBG_OK(p.status, ui.split < p.s_tail && (p.s_tail == 2 || p.s_tail == 4 || p.s_tail == 8)))
+        cm_send<D>(sb + C::kOffQ, sb + C::kOffCm, p.s_tail, ui.split, X * kTileM + r, tO, n, m_ref, l);
       cluster_sync();   // all partials of this CTA's rows have landed
       {
         const uint32_t rb = sb + C::kOffQ, mb2 = sb + C::kOffCm, stg = sb + C::kOffQ + C::kCmStage;
@@ -813,6 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t obase = E == Elem::E4M3 ? sb + C::kOffKV + X * C::kOTileBytes
                                              : sb + C::kOffQ + X * C::kTileBytes;
       constexpr Elem OE = kOutElem<E>;
+      if (ok && !FA_DBG_OK(p.status, smem_in(obase, C::kOBoxes * C::kBoxBytes, sb, s_hi) && bh < p.n_bh))
+        ok = false;   // FA_DEBUG: reported; nothing stored
       if (ok) {
         const float inv = l > 0.f ? p.o_scale / l : 0.f;
 #pragma unroll 1
@@ -853,6 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K/V ring, one TMA store) and (m, l) of this key range to the workspace
       const uint32_t pbase = sb + C::kOffKV + X * C::kPartTileBytes;
       const int prow0 = slot * kBlockRows + X * kTileM;
+      if (ok && !FA_DBG_OK(p.status, smem_in(pbase, C::kPartTileBytes, sb + C::kOffKV, sb + C::kOffBar) &&
+                                         slot >= 0 && slot < p.n_tail * p.s_tail))
+        ok = false;   // FA_DEBUG: reported; nothing stored
       if (ok) {
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {

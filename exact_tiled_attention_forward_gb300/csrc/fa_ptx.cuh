@@ -18,8 +18,36 @@
 // device status codes (kept in one int; the first error of a launch sticks)
 #define FA_DEV_OK 0
 #define FA_DEV_TIMEOUT 1
+#define FA_DEV_BOUNDS 2
 
 namespace fa {
+
+// Bounds checks of FA_DEBUG builds (the stand-in for a memory checker): a
+// failed check records FA_DEV_BOUNDS in the status word and the caller skips
+// the access, so an out-of-range tensor-memory column, shared-memory offset or
+// global row is reported instead of touched. Release builds compile the checks
+// away (FA_DBG_OK is the constant true). Conditions guarding a warp-collective
+// instruction are warp-uniform.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool dbg_ok(int* status, bool ok) {
+  if (!ok && status) atomicCAS(status, FA_DEV_OK, FA_DEV_BOUNDS);
+  return ok;
+}
+#define FA_DBG_OK(status, cond) ::fa::dbg_ok((status), (cond))
+#else
+#define FA_DBG_OK(status, cond) true
+#endif
+// A tensor-memory access of ncols columns at address a (relative to the CTA's
+// allocation: lane in the upper 16 bits, column in the lower) stays inside
+// 128 lanes x cols columns and starts at a warp's lane quadrant.
+__device__ __forceinline__ bool tmem_in(uint32_t a, uint32_t ncols, uint32_t cols = 512) {
+  const uint32_t lane = a >> 16, col = a & 0xFFFFu;
+  return (lane & 31u) == 0 && lane < 128u && col + ncols <= cols;
+}
+// A shared-memory access of `bytes` at shared address a lies in [lo, hi).
+__device__ __forceinline__ bool smem_in(uint32_t a, uint32_t bytes, uint32_t lo, uint32_t hi) {
+  return a >= lo && a + bytes <= hi;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -22,8 +22,38 @@ __global__ void __launch_bounds__(32) fa_selftest_wait_kernel(int* status, unsig
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status, timeout_ns);
 }
 
+// One thread runs a bounds check whose condition is false (no memory is
+// touched): an FA_DEBUG build records FA_DEV_BOUNDS in the status word.
+__global__ void __launch_bounds__(32) fa_selftest_bounds_kernel(int* status) {
+  if (threadIdx.x == 0) {
+    volatile uint32_t col = 512;   // one column past the allocation
+    if (FA_DBG_OK(status, tmem_in(col, 32))) { /* the access a check guards would go here */ }
+  }
+}
+
 }  // namespace
 }  // namespace fa
+
+extern "C" int fa_debug_build(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+extern "C" int fa_selftest_bounds(void* stream) {
+#ifndef FA_DEBUG
+  (void)stream;
+  return FA_ERR_UNSUPPORTED;
+#else
+  int* status = fa::device_status_ptr();
+  if (!status) return fa::cuda_fail(cudaGetLastError());
+  const cudaError_t e = fa::launch_kernel(fa::fa_selftest_bounds_kernel, dim3(1), dim3(32), 0,
+                                          static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? FA_OK : fa::cuda_fail(e);
+#endif
+}
 
 extern "C" int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
   if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FA_ERR_INVALID_ARG;

@@ -63,7 +63,8 @@ typedef enum {
   FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   FA_ERR_NO_MEMORY = -4,   /* stream-ordered workspace allocation failed, or workspace too small */
   FA_ERR_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (device status word) */
-  FA_ERR_TOO_LARGE = -6    /* fa_forward_noalloc: needs more than its static scratch holds */
+  FA_ERR_TOO_LARGE = -6,   /* fa_forward_noalloc: needs more than its static scratch holds */
+  FA_ERR_BOUNDS = -7       /* FA_DEBUG builds: a device-side bounds check failed (status word) */
 } fa_status;
 
 /* Element type of q, k, v and o for the entry points that take one. */
@@ -269,15 +270,29 @@ int fa_forward_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causa
  * out of range, FA_ERR_CUDA on a launch failure. */
 int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 
+/* 1 if this library was compiled with FA_DEBUG (device-side bounds checks:
+ * every tensor-memory column range, shared-memory offset and global row index
+ * the kernels use is checked first; a failed check records FA_ERR_BOUNDS in the
+ * device status word and the access is skipped, nothing faults), else 0. No
+ * counterpart on the pages: it stands in for a memory checker. */
+int fa_debug_build(void);
+
+/* FA_DEBUG builds: enqueue on `stream` one CTA whose single bounds check fails
+ * by construction (no memory is touched), so fa_device_status then reports
+ * FA_ERR_BOUNDS: a test of the recording path. Release builds return
+ * FA_ERR_UNSUPPORTED and enqueue nothing. */
+int fa_selftest_bounds(void* stream);
+
 /* Static description of an fa_status code. Never NULL. */
 const char* fa_status_string(int status);
 
 /* The cudaError_t of the last CUDA failure this thread saw inside libfa (0 if none). */
 int fa_get_last_cuda_error(void);
 
-/* Synchronises the current device, then returns FA_OK or FA_ERR_TIMEOUT from
- * the device status word that kernels set when a bounded wait runs out;
- * `reset` != 0 clears the word afterwards. FA_ERR_CUDA if synchronisation fails. */
+/* Synchronises the current device, then returns FA_OK, FA_ERR_TIMEOUT (a
+ * kernel's bounded wait ran out) or FA_ERR_BOUNDS (FA_DEBUG builds: a bounds
+ * check failed) from the device status word; `reset` != 0 clears the word
+ * afterwards. FA_ERR_CUDA if synchronisation fails. */
 int fa_device_status(int reset);
 
 /* Library version, (major << 16) | minor. */

@@ -26,7 +26,7 @@ def lib():
 def test_header_symbols_exported(lib):
     names = fa.header_functions()
     assert set(names) == {"fa_forward", "fa_forward_fp16", "fa_forward_fp8", "fa_forward_host",
-                          "fa_forward_host_packed",
+                          "fa_forward_host_packed", "fa_debug_build", "fa_selftest_bounds",
                           "fa_backward", "fa_decode_paged",
                           "fa_forward_noalloc",
                           "fa_naive_forward",
@@ -72,8 +72,15 @@ def test_single_gpu_forward_refuses_multi_process_jobs(lib, monkeypatch):
     assert f(Q, K, V, Q, L, 1, 2, 1, 64, 64, 128, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
 
 
+def test_debug_build_switch(lib):
+    # the default library has no bounds checks and refuses their self-test
+    assert lib.fa_debug_build() == 0
+    assert lib.fa_selftest_bounds(None) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6, 7):
+    assert fa.fa_status_string(-7) == "a bounds check of the FA_DEBUG build failed"
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 7):
         s = fa.fa_status_string(code)
         assert isinstance(s, str) and s
     assert fa.fa_status_string(-5) == "kernel wait timed out"
