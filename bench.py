@@ -50,6 +50,8 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_fwd.cu",
                       "exact_tiled_attention_forward_gb300/csrc/fa_fwd_kernel.cuh",
                       "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
+    "fa_fwd_tile_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_fwd_d256.cu",
+                           "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
     "fa_decode_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_decode.cu",
                          "exact_tiled_attention_forward_gb300/csrc/fa_ptx.cuh"],
     "fa_bwd_kernel": ["exact_tiled_attention_forward_gb300/csrc/fa_bwd.cu",
@@ -902,7 +904,8 @@ def main():
         peak = float(peaks["bf16_tflops"]) * (2.0 if args.dtype == "e4m3" else 1.0)
         achieved = a_flops / 1e12 / (ms_per_step * 1e-3)
         roof = {"bound": "tensor", "unit": "TFLOP/s"}
-    traffic = (profiled_traffic(args.workload + ("_e4m3" if args.dtype == "e4m3" else ""))
+    main_kernel = "fa_fwd_tile_kernel" if d == 256 else "fa_fwd_kernel"
+    traffic = (profiled_traffic(args.workload + ("_e4m3" if args.dtype == "e4m3" else ""), main_kernel)
                if args.impl == "fused" else None)
     if args.dtype == "bf16" or decode_cfg:
         peak_src_note = f"{peak_src} (burst)"
@@ -914,7 +917,7 @@ def main():
                  "traffic": traffic,
                  "peak_source": peak_src_note,
                  "algorithmic_per_launch": a_bytes if decode_cfg else a_flops,
-                 "kernel": "fa_fwd_kernel" if args.impl == "fused" else "naive (3 kernels)"})
+                 "kernel": main_kernel if args.impl == "fused" else "naive (3 kernels)"})
 
     cpu = None
     if args.cpu_budget > 0 and world == 1:
