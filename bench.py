@@ -330,7 +330,12 @@ def time_decode(fa, torch, dev, flush, stream, steps, warmup, world, dtype="bf16
         f1.record(stream)
     torch.cuda.synchronize()
     fms = R.slowest_rank_ms(sum(f0.elapsed_time(f1) for f0, f1 in evs) / steps, world, dev)
-    return {"ms": ms, "gbs": R.whole_job_rate(a_bytes / 1e9, 1, ms, world), "bytes": a_bytes,
+    plan = fa.fa_forward_plan(B, Hq, Hkv, Nq, Nk, d, False)
+    parts = plan["ctas"] // (B * Hkv)
+    split = (f"128-key chunks, {-(-((Nk + 127) // 128) // parts)} consecutive chunks per CTA, "
+             f"{parts} CTAs per (batch, KV head), partials merged "
+             + ("inside thread-block clusters" if plan["launches"] == 1 else "by a second kernel"))
+    return {"ms": ms, "gbs": R.whole_job_rate(a_bytes / 1e9, 1, ms, world), "bytes": a_bytes, "split": split,
             "flushed_ms": fms, "flushed_gbs": R.whole_job_rate(a_bytes / 1e9, 1, fms, world),
             "launches": fused_launches_per_step(fa, cfg)}
 
@@ -957,6 +962,7 @@ def main():
                              "before it, outside the events")},
         "decode": None if decode is None else {
             "workload": DECODE_WORKLOAD, "value": decode["gbs"], "unit": "GB/s",
+            "split": decode["split"],
             "ms_per_step": decode["ms"], "steps": args.decode_steps,
             "l2": "inputs larger than L2: two input sets of 537 MB used in turn, back to back",
             "flushed": {"value": decode["flushed_gbs"], "unit": "GB/s",
