@@ -12,7 +12,8 @@
 //    sees no key, and on the padding rows of the last tile) and D, into arrays
 //    padded to whole 128-row tiles.
 //  * fa_bwd_kernel, whose CTAs take one of two roles (they share no data, so
-//    both run side by side in one grid, dK/dV CTAs first):
+//    both run side by side in one grid, the dK/dV CTAs of a KV head followed by
+//    the dQ CTAs of its query heads, so its tiles are read from L2 the second time):
 //    - dK/dV: one CTA per (batch, KV head, block of 128 keys). K and V of the
 //      block stay in shared memory; the CTA walks the query tiles of every
 //      query head that reads the KV head (GQA sums them in place, no atomics).
@@ -639,19 +640,30 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
   }
 }
 
-// One launch for both halves of the work: CTAs [0, B*H_kv*n_kb) are dK/dV
-// CTAs, the rest dQ CTAs; the two roles share no data and run side by side,
-// longest work first within each role.
+// One launch for both halves of the work. CTAs come in groups, one per KV
+// head: its n_kb dK/dV CTAs, then the G * n_qt dQ CTAs of its query heads, so
+// the second role reads the head's Q, K, V and dO tiles while they are still in
+// L2 (the whole first role before the whole second left them to be read from
+// DRAM twice when many heads run). Within each role of a group the longest work
+// goes first (key blocks ascending, query tiles descending: under a causal mask
+// those are the long ones), the group's query heads interleaved. A finer
+// alternation (dK/dV block i, dQ rank i, ...) measured slower.
 template <int D, Elem E>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const BwdParams p) {
-  const int n_kv = p.B * p.H_kv * p.n_kb;
-  if ((int)blockIdx.x < n_kv)
-    bwd_dkdv_cta<D, E>(tmQ, tmK, tmV, tmdO, p, (int)blockIdx.x);
-  else
-    bwd_dq_cta<D, E>(tmQ, tmK, tmV, tmdO, p, (int)blockIdx.x - n_kv);
+  const int per = p.n_kb + p.G * p.n_qt;        // CTAs of one KV head's group
+  const int grp = (int)blockIdx.x / per;        // = b * H_kv + KV head
+  const int w = (int)blockIdx.x - grp * per;
+  if (w < p.n_kb) {
+    bwd_dkdv_cta<D, E>(tmQ, tmK, tmV, tmdO, p, grp * p.n_kb + w);
+  } else {
+    const int idx = w - p.n_kb;
+    // rank idx / G of query head G * (KV head) + idx % G
+    const int gi = idx % p.G, rank = idx / p.G;
+    bwd_dq_cta<D, E>(tmQ, tmK, tmV, tmdO, p, (grp * p.G + gi) * p.n_qt + rank);
+  }
 }
 
 template <int D, Elem E>
