@@ -206,7 +206,7 @@ def fa_forward_fp8(q, k, v, descale, causal: bool = False, scale: float | None =
     """Fused forward on FP8 E4M3 inputs: q, k, v hold E4M3 codes (torch.uint8 or
     torch.float8_e4m3fn, one byte each) standing for code * factor, with
     ``descale = (factor_q, factor_k, factor_v)``. Returns ``(o, lse)``: o BF16,
-    lse FP32. d must be 128."""
+    lse FP32. d must be 64 or 128."""
     import torch
     allowed = {torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)}
     for name, t in (("q", q), ("k", k), ("v", v)):

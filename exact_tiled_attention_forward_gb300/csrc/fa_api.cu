@@ -280,12 +280,15 @@ bool make_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
                      uint64_t outer, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  // rows of 64 bytes (d = 64) take 64-byte boxes with the 64-byte swizzle
+  const bool narrow = inner < 128;
   cuuint64_t dims[3] = {inner, rows, outer};
   cuuint64_t strides[2] = {inner, inner * rows};
-  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t box[3] = {narrow ? 64u : 128u, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -374,7 +377,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   const Shape s{B, H_q, H_kv, N_q, N_k, d};
   int st = validate_shape(s);
   if (st != FA_OK) return st;
-  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (fp8 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   st = validate(q, k, v, o, lse, s, scale, true, fp8 ? 1 : 2);
   if (st != FA_OK) return st;
   if ((long long)B * H_q * N_q == 0) return FA_OK;

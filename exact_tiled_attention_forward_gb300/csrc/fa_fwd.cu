@@ -1,5 +1,5 @@
 // Fused prefill forward of libfa: instantiates the plain kernel of
-// fa_fwd_kernel.cuh (BF16 and FP16 with d = 64 and 128, FP8 E4M3 with d = 128)
+// fa_fwd_kernel.cuh (BF16, FP16 and FP8 E4M3, d = 64 and 128)
 // and its merge kernel.
 #include "fa_fwd_kernel.cuh"
 
@@ -43,7 +43,8 @@ size_t fwd_smem_bytes(int d) {
 cudaError_t launch_fwd(int d, const FwdMaps& m, const FwdParams& p, int units, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
   if (p.elem == (int)Elem::E4M3)
-    return d == 128 ? launch_fwd_t<128, Elem::E4M3>(m, p, units, stream) : cudaErrorInvalidValue;
+    return d == 128 ? launch_fwd_t<128, Elem::E4M3>(m, p, units, stream)
+                    : launch_fwd_t<64, Elem::E4M3>(m, p, units, stream);
   if (p.elem == (int)Elem::F16)
     return d == 128 ? launch_fwd_t<128, Elem::F16>(m, p, units, stream)
                     : launch_fwd_t<64, Elem::F16>(m, p, units, stream);

@@ -89,11 +89,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D, Elem E = Elem::BF16>
 struct Cfg {
   static constexpr int kEsz = E == Elem::E4M3 ? 1 : 2;   // bytes per Q, K, V element
-  static constexpr int kBoxCols = 128 / kEsz;             // elements in one 128-byte box row
-  static constexpr int kBoxes = D * kEsz / 128;           // 128-byte boxes per tile row
-  static_assert(kBoxes >= 1, "a tile row holds at least one 128-byte box");
+  // Q, K, V tiles: boxes of 128 rows with a 128-byte swizzle (64-byte rows,
+  // and a 64-byte swizzle, for FP8 at d = 64, whose rows are 64 bytes long)
+  static constexpr int kRowBytes = D * kEsz;
+  static constexpr int kSwz = kRowBytes < 128 ? kRowBytes : 128;   // swizzle span = box row bytes
+  static_assert(kSwz == 64 || kSwz == 128, "64- or 128-byte swizzle");
+  static constexpr int kBoxCols = kSwz / kEsz;            // elements in one box row
+  static constexpr int kBoxes = kRowBytes / kSwz;         // boxes per tile row
+  static constexpr int kBoxBytes = 128 * kSwz;            // 128 rows x kSwz bytes
+  static constexpr int kKPerBox = kSwz / 32;              // S MMAs (32 bytes of K each) per box
   static constexpr int kOBoxes = D / 64;                  // 64-column boxes of a 16-bit O row
-  static constexpr int kBoxBytes = 128 * 128;             // 128 rows x 128 bytes
+  static constexpr int kStgBoxBytes = 128 * 128;          // staging boxes (O, partials): 128 x 128 bytes
   static constexpr int kTileBytes = 128 * D * kEsz;       // one Q, K or V tile
   static constexpr int kOTileBytes = 128 * D * 2;         // one 16-bit O tile
   static constexpr int kPartTileBytes = 128 * D * 4;      // one FP32 partial tile
@@ -123,7 +129,11 @@ struct Cfg {
   static constexpr int kCmRows = kBlockRows;                  // (m, l) of every row, by sender
   static constexpr int kOffCm = (kOffMisc + 64 + 15) & ~15;
   static constexpr int kCmStage = kBlockRows * D * 4;         // after the FP32 receive buffer
-  static constexpr int kSmemBytes = kOffCm + kCmRows * 8 + 1024;  // + alignment slack
+  // + alignment slack; at least 120 KB, so that two CTAs never share an SM: each
+  // allocates all 512 TMEM columns, and a second allocation on the SM would
+  // wait for the first CTA to finish (FP8 tiles at d = 64 need only ~80 KB)
+  static constexpr int kSmemUsed = kOffCm + kCmRows * 8 + 1024;
+  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
   static_assert(kCmStage + 128 * D * 2 <= kOffBar, "merge buffers must fit in the Q tiles and the K/V ring");
   static_assert(2 * kPartTileBytes <= kStages * kTileBytes, "both partial tiles fit in the K/V ring");
   static_assert(kEsz == 2 || 2 * kOTileBytes <= kStages * kTileBytes, "FP8: O staged in the K/V ring");
@@ -618,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // start-address field (16-byte units) of the low word, so issuing stays
         // ahead of the tensor core.
         constexpr uint32_t kStageStep = (uint32_t)(C::kTileBytes >> 4);
-        constexpr uint32_t kHi = desc_sw128_hi(1024);
+        // 8-row swizzle atoms: SBO = 8 rows of the box
+        constexpr uint32_t kHi = C::kSwz == 128 ? desc_sw128_hi(1024) : desc_sw64_hi(512);
         const uint32_t lq0 = desc_sw128_lo(sb + C::kOffQ, 16);
         const uint32_t lk0 = desc_sw128_lo(sb + C::kOffKV, 16);
         const uint32_t lv0 = desc_sw128_lo(sb + C::kOffKV, C::kBoxBytes);
@@ -631,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < C::kSKSteps; ++kk) {
             constexpr uint32_t kBox16 = C::kBoxBytes >> 4;
-            const uint32_t off = (uint32_t)(kk >> 2) * kBox16 + (uint32_t)(kk & 3) * 2u;
+            const uint32_t off = (uint32_t)(kk / C::kKPerBox) * kBox16 + (uint32_t)(kk % C::kKPerBox) * 2u;
             if constexpr (E == Elem::E4M3)
               mma_ss_lh_w_f8(d, a0 + off, kHi, b0 + off, kHi, idS, kk > 0 ? 1u : 0u);
             else
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V rows from kPVKeys*kk on, 128 bytes each)
         auto issue_PV = [&](int X, int st, bool acc, int h) {   // keys 64h .. 64h+63
           constexpr int kPer = 64 / C::kPVKeys;
-          constexpr uint32_t kVStep = (uint32_t)(C::kPVKeys * 128) >> 4;
+          constexpr uint32_t kVStep = (uint32_t)(C::kPVKeys * C::kSwz) >> 4;   // kPVKeys box rows
           if (!FA_DBG_OK(p.status, st < C::kStages && tmem_in(C::tm_o(X), D) &&
                                        tmem_in(C::tm_s(X), 2 * C::kPHalfCols)))
             return;
@@ -830,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t obase = E == Elem::E4M3 ? sb + C::kOffKV + X * C::kOTileBytes
                                              : sb + C::kOffQ + X * C::kTileBytes;
       constexpr Elem OE = kOutElem<E>;
-      if (ok && !FA_DBG_OK(p.status, smem_in(obase, C::kOBoxes * C::kBoxBytes, sb, s_hi) && bh < p.n_bh))
+      if (ok && !FA_DBG_OK(p.status, smem_in(obase, C::kOBoxes * C::kStgBoxBytes, sb, s_hi) && bh < p.n_bh))
         ok = false;   // FA_DEBUG: reported; nothing stored
       if (ok) {
         const float inv = l > 0.f ? p.o_scale / l : 0.f;
@@ -844,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = 0.f;
           }
-          const uint32_t rowaddr = obase + (uint32_t)(cc >> 6) * C::kBoxBytes + (uint32_t)r * 128u;
+          const uint32_t rowaddr = obase + (uint32_t)(cc >> 6) * C::kStgBoxBytes + (uint32_t)r * 128u;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const uint32_t ch = (uint32_t)(((cc & 63) >> 3) + g);   // 16-byte chunk in the row
@@ -863,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (all_ok && r == 0 && tile_first_row < p.N_q) {   // rows past N_q are clipped by the TMA
 #pragma unroll
         for (int bx = 0; bx < C::kOBoxes; ++bx)
-          tma_store_3d(&tmO, obase + bx * C::kBoxBytes, bx * 64, tile_first_row, bh);
+          tma_store_3d(&tmO, obase + bx * C::kStgBoxBytes, bx * 64, tile_first_row, bh);
         bulk_commit();
         bulk_wait_read0();
       }
@@ -886,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = 0.f;
           }
-          const uint32_t rowaddr = pbase + (uint32_t)(cc >> 5) * C::kBoxBytes + (uint32_t)r * 128u;
+          const uint32_t rowaddr = pbase + (uint32_t)(cc >> 5) * C::kStgBoxBytes + (uint32_t)r * 128u;
 #pragma unroll
           for (int g = 0; g < 8; ++g)
             st_shared_v4(rowaddr + (((uint32_t)g ^ (uint32_t)(r & 7)) << 4), __float_as_uint(ov[4 * g]),
@@ -900,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool all_ok = named_bar_and(1 + X, 128, ok);
       if (all_ok && r == 0) {
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) tma_store_2d(&tmP, pbase + bx * C::kBoxBytes, bx * 32, prow0);
+        for (int bx = 0; bx < D / 32; ++bx) tma_store_2d(&tmP, pbase + bx * C::kStgBoxBytes, bx * 32, prow0);
         bulk_commit();
         bulk_wait_read0();
       }

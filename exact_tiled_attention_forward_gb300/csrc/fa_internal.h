@@ -182,7 +182,8 @@ extern thread_local int g_last_cuda_error;
 // 3-D BF16 tensor map over [outer][rows][inner] with a {64, 128, 1} box, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t outer, uint64_t row_stride_elems, uint32_t box_rows);
-// 3-D 8-bit tensor map over [outer][rows][inner] with a {128, box_rows, 1} box, 128-byte swizzle.
+// 3-D 8-bit tensor map over [outer][rows][inner] with a {128, box_rows, 1} box and
+// 128-byte swizzle ({64, box_rows, 1} and 64-byte swizzle when inner < 128).
 bool make_tmap_u8_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                      uint64_t outer, uint32_t box_rows);
 

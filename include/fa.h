@@ -38,7 +38,7 @@
  *  - scale must be finite and > 0 (1/sqrt(d) is the usual value).
  *  - d must be 64 or 128, or 256 for the forward entry points fa_forward,
  *    fa_forward_fp16, fa_forward_noalloc and fa_forward_host[_packed]
- *    (FA_ERR_UNSUPPORTED otherwise; FP8 inputs: 128).
+ *    (FA_ERR_UNSUPPORTED otherwise; FP8 inputs: 64 or 128).
  *  - stream: a cudaStream_t (NULL = legacy default stream). Calls are
  *    asynchronous: they return once the work is enqueued. Argument errors are
  *    reported before anything is enqueued. Launch errors return FA_ERR_CUDA
@@ -119,7 +119,7 @@ int fa_forward_fp16(const void* q, const void* k, const void* v, void* o, float*
  * FP32 accumulation), the factors of Q and K and `scale` folded into the
  * exponent; P rounded to E4M3 (nearest even, at most 2^8 against the row's
  * reference max) for the P V product; O multiplied by descale_v / l in FP32
- * and rounded to BF16. d must be 128 (FA_ERR_UNSUPPORTED otherwise). Every
+ * and rounded to BF16. d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise). Every
  * request runs the prefill kernel (including one-query decode shapes). Pointers,
  * alignment, overlap, workspace and error codes as fa_forward. */
 int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,

@@ -155,7 +155,7 @@ def test_fp8_rejects(lib):
     def f(q=Q, k=K, v=V, o=O, l=L, Hq=2, Hkv=1, Nq=64, d=128, scale=0.1, ds=(1.0, 1.0, 1.0)):
         return lib.fa_forward_fp8(q, k, v, o, l, 1, Hq, Hkv, Nq, 64, d, 0, scale, *ds, None)
     assert f(Hq=3, Hkv=2) == fa.FA_ERR_INVALID_ARG                       # H_q % H_kv
-    assert f(d=64) == fa.FA_ERR_UNSUPPORTED                               # FP8: d = 128 only
+    assert f(d=256) == fa.FA_ERR_UNSUPPORTED                              # FP8: d = 64 or 128
     for bad in ((0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, math.inf), (1.0, math.nan, 1.0)):
         assert f(ds=bad) == fa.FA_ERR_INVALID_ARG                         # factors finite, > 0
     assert f(ds=(1e30, 1e30, 1.0)) == fa.FA_ERR_INVALID_ARG                # scale * factors overflows

@@ -103,8 +103,37 @@ def test_fp8_deterministic(fa):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_fp8_rejects_head_dim_64(fa):
+def test_fp8_rejects_head_dim_256(fa):
     import torch
-    q = torch.zeros((1, 1, 64, 64), dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 1, 64, 256), dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FaError):
         fa.fa_forward_fp8(q, q, q, (1.0, 1.0, 1.0))
+
+
+# head dimension 64: 64-byte rows, 64-byte swizzled tiles
+D64 = [
+    (1, 1, 1, 256, 256, False, 0.0),       # the small workload (one head, N = 256, d = 64)
+    (1, 1, 1, 17, 17, True, 0.0),
+    (1, 2, 1, 255, 255, True, 0.01),
+    (2, 8, 2, 300, 700, True, 0.01),       # GQA, N_q < N_k
+    (1, 4, 4, 600, 200, True, 0.0),        # rows that see no key
+    (1, 1, 1, 2000, 3000, False, 0.0),     # split key ranges
+]
+
+
+@pytest.mark.parametrize("shape", D64, ids=lambda s: "x".join(map(str, s[:5])) + ("c" if s[5] else ""))
+def test_fp8_head_dim_64(fa, shape):
+    B, Hq, Hkv, Nq, Nk, causal, frac = shape
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, 64, causal=causal, seed=34, k_row_frac=frac, dtype="e4m3")
+    _check(fa, a)
+
+
+def test_fp8_tiny_workload(fa):
+    _check(fa, I.make_workload("tiny_n256_d64", dtype="e4m3"))
+
+
+@pytest.mark.parametrize("cluster_merge", [True, False], ids=["cluster", "kernel"])
+def test_fp8_head_dim_64_split_merge_modes(fa, cluster_merge, monkeypatch):
+    monkeypatch.setenv("FA_CLUSTER_MERGE", "1" if cluster_merge else "0")
+    a = I.make_inputs(1, 1, 1, 2048, 8192, 64, causal=False, seed=35, k_row_frac=0.01, dtype="e4m3")
+    _check(fa, a)
