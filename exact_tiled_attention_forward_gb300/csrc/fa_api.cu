@@ -402,6 +402,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     p.n_qt = (N_q + 127) / 128;
     p.n_kv_tiles = (N_k + 127) / 128;
     p.elem = elem;
+    p.hgroup = causal ? causal_head_group(H_q, H_kv, N_k, d, B * H_q) : 1;
     p.c = scale * 1.4426950408889634f;
     p.lse = lse;
     p.status = status;

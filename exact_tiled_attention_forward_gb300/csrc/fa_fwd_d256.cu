@@ -80,11 +80,28 @@ struct LagD {
 
 __device__ __forceinline__ int mini(int a, int b) { return a < b ? a : b; }
 
-// Query tile of unit u: head-major; causal tiles longest first within a head.
+// Query tile of unit u. Non-causal: head-major (a head's tiles adjacent, so its
+// K and V are read from DRAM once). Causal: tiles differ in length and CTAs are
+// handed out in order, so heads are taken in groups of p.hgroup whose K and V
+// fit in L2 together, and inside a group the tiles run longest first with the
+// group's heads interleaved (the last tile of every head, then the one before,
+// ...); head-major order would leave the longest tiles of the last heads to
+// start at the very end.
 __device__ __forceinline__ void tile_of(const D256Params& p, int u, int& bh, int& qt) {
-  bh = u / p.n_qt;
-  const int i = u - bh * p.n_qt;
-  qt = p.causal ? p.n_qt - 1 - i : i;
+  if (!p.causal) {
+    bh = u / p.n_qt;
+    qt = u - bh * p.n_qt;
+    return;
+  }
+  const int g = p.hgroup;
+  const int per = g * p.n_qt;
+  const int grp = u / per;
+  const int w = u - grp * per;
+  const int n_bh = p.B * p.H_q;
+  const int gh = mini(g, n_bh - grp * g);   // heads in this group (the last may have fewer)
+  const int rank = w / gh;
+  bh = grp * g + (w - rank * gh);
+  qt = p.n_qt - 1 - rank;
 }
 
 // Key tiles query tile qt needs: [0, n). Fully masked tiles are never loaded.

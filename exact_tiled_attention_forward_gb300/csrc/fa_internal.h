@@ -76,6 +76,7 @@ struct D256Params {
   int n_qt;         // ceil(N_q / 128) query tiles per (b, h)
   int n_kv_tiles;   // ceil(N_k / 128)
   int elem;         // 0 = BF16, 1 = FP16
+  int hgroup;       // causal tile order: heads per group (>= 1)
   float c;          // scale * log2(e)
   float* lse;       // fp32 [B][H_q][N_q] or nullptr
   int* status;

@@ -93,3 +93,16 @@ def test_d256_deterministic_and_noalloc(fa):
     torch.cuda.synchronize()
     assert np.array_equal(bf16_dev_to_f64(o3), o1)
     assert np.array_equal(l3.cpu().numpy().astype(np.float64), l1)
+
+
+@pytest.mark.parametrize("group", [None, "1", "3"], ids=["default", "g1", "g3"])
+def test_d256_causal_head_groups(fa, group, monkeypatch):
+    # causal tiles run longest first across groups of heads; groups of 3 leave a
+    # short last group, and every tile must still be written exactly once
+    if group is None:
+        monkeypatch.delenv("FA_CAUSAL_HEAD_GROUP", raising=False)
+    else:
+        monkeypatch.setenv("FA_CAUSAL_HEAD_GROUP", group)
+    a = I.make_inputs(2, 10, 5, 700, 900, 256, causal=True, seed=43, k_row_frac=0.01)
+    o, lse = _run(fa, a)
+    compare(o, lse, *run_oracle(a))
