@@ -265,12 +265,15 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         const int q0 = t * kT;
         const uint32_t sq = sb + C::kOffStages + st * C::kStageBytes;
         mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes + 2 * C::kVecBytes);
+        const size_t vo = (size_t)bhq * p.nq_pad + q0;
+        // FA_DEBUG: the stage lies in shared memory, the tile and its two vectors in their tensors
+        if (!FA_DBG_OK(p.status, st < C::kStages && q0 + kT <= p.nq_pad && bhq < p.B * p.H_q))
+          continue;   // reported, not loaded (the consumer's bounded wait then gives up)
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_3d(sq + bx * C::kBoxBytes, &tmQ, bar(C::kBarFull + st), bx * 64, q0, bhq);
           tma_load_3d(sq + C::kTileBytes + bx * C::kBoxBytes, &tmdO, bar(C::kBarFull + st), bx * 64, q0, bhq);
         }
-        const size_t vo = (size_t)bhq * p.nq_pad + q0;
         bulk_load_1d(sq + 2 * C::kTileBytes, p.lse2 + vo, C::kVecBytes, bar(C::kBarFull + st));
         bulk_load_1d(sq + 2 * C::kTileBytes + C::kVecBytes, p.dsum + vo, C::kVecBytes, bar(C::kBarFull + st));
       }
@@ -385,6 +388,10 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
           break;
         const uint32_t cc = 64u * h + 32u * grp;   // this warpgroup's 32 columns = rows
         float s[32], dp[32];
+        if (!FA_DBG_OK(p.status, tmem_in(lane_base + C::kTmS + cc, 32) && tmem_in(lane_base + C::kTmP + cc, 32))) {
+          ok = false;   // FA_DEBUG: reported; this step is not processed
+          break;
+        }
         tmem_ld32(tS + cc, s);
         tmem_ld32(tP + cc, dp);
         tmem_wait_ld();
@@ -409,6 +416,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       ok = mbar_wait_w(bar(C::kBarDone), 0, s_abort, p.status);
       tc_fence_after();
     }
+    if (ok && !FA_DBG_OK(p.status, bhk < p.B * p.H_kv && tmem_in(lane_base + C::kTmA, D) &&
+                                      tmem_in(lane_base + C::kTmB, D)))
+      ok = false;   // FA_DEBUG: reported; nothing stored
     if (ok) {   // warp-uniform; keys past N_k (a ragged last block) load but do not store
       const bool valid = key < p.N_k;
       const size_t row = ((size_t)bhk * p.N_k + (valid ? key : 0)) * D;
@@ -499,6 +509,8 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
         if (!mbar_wait(bar(C::kBarEmpty + st), ph ^ 1u, s_abort, p.status)) break;
         const uint32_t sk = sb + C::kOffStages + st * C::kStageBytes;
         mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
+        if (!FA_DBG_OK(p.status, st < C::kStages && j < p.n_kb && bhk < p.B * p.H_kv))
+          continue;   // FA_DEBUG: reported, not loaded
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_3d(sk + bx * C::kBoxBytes, &tmK, bar(C::kBarFull + st), bx * 64, j * kT, bhk);
@@ -603,6 +615,10 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
         const uint32_t cc = 64u * h + 32u * grp;   // this warpgroup's 32 columns = keys
         const int key0 = j * kT + (int)cc;
         float s[32], dp[32];
+        if (!FA_DBG_OK(p.status, tmem_in(lane_base + C::kTmS + cc, 32) && tmem_in(lane_base + C::kTmP + cc, 32))) {
+          ok = false;   // FA_DEBUG: reported; this step is not processed
+          break;
+        }
         tmem_ld32(tS + cc, s);
         tmem_ld32(tP + cc, dp);
         tmem_wait_ld();
@@ -625,6 +641,8 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       ok = mbar_wait_w(bar(C::kBarDone), 0, s_abort, p.status);
       tc_fence_after();
     }
+    if (ok && !FA_DBG_OK(p.status, bhq < p.B * p.H_q && tmem_in(lane_base + C::kTmA, D)))
+      ok = false;   // FA_DEBUG: reported; nothing stored
     if (ok) {   // warp-uniform; rows past N_q (a ragged last tile) load but do not store
       const bool valid = row < p.N_q;   // warpgroup g writes columns [g D/2, (g+1) D/2)
       store_row<D, E>(tmem + lane_base + C::kTmA,

@@ -1,8 +1,9 @@
 """The FA_DEBUG build of libfa (device-side bounds checks that record a status
 code and skip the access, the stand-in for a memory checker): it builds, its
 self-test reports FA_ERR_BOUNDS through the status word, and the small and
-ragged shapes, split plans (both merge routes), decode shapes, d = 256 and FP8
-inputs all run under it with no bounds report and oracle-exact results."""
+ragged shapes, split plans (both merge routes), decode shapes, d = 256, FP8
+inputs and the backward all run under it with no bounds report and results
+within the oracle's tolerances."""
 import ctypes
 
 import numpy as np
@@ -98,3 +99,28 @@ def test_fp8_under_bounds_checks(dbg):
     o, lse = _forward(dbg, a, fp8=True)
     o_ref, lse_ref, a_ref, e_ref = run_oracle_fp8(a)
     compare(o, lse, o_ref, lse_ref, a_ref, tol_rel=TOL_REL_L2_O_FP8, elem="e4m3", fp8_e=e_ref)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 17, 17, 128, True, "bf16"), (1, 2, 1, 300, 700, 128, True, "bf16"),
+                                   (1, 2, 2, 600, 200, 64, True, "bf16"), (2, 4, 2, 513, 513, 64, False, "f16")],
+                         ids=["tiny_causal", "gqa_ragged", "nq_gt_nk_d64", "f16_d64"])
+def test_backward_under_bounds_checks(dbg, shape):
+    import torch
+    import test_gpu_backward as TB
+    from exact_tiled_attention_forward_gb300 import FA_DTYPE_BF16, FA_DTYPE_FP16
+    B, H_q, H_kv, N_q, N_k, d, causal, dtype = shape
+    a = I.make_inputs(B, H_q, H_kv, N_q, N_k, d, causal=causal, seed=9, dtype=dtype)
+    do = I.grad_output(a, seed=9)
+    o16, lse32 = TB._forward_inputs(a)
+    q, k, v, o, dod = to_dev(a.q), to_dev(a.k), to_dev(a.v), to_dev(o16), to_dev(do)
+    lse = torch.from_numpy(np.ascontiguousarray(lse32)).cuda()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = dbg.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dod.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H_q, H_kv, N_q, N_k, d, int(causal),
+                         a.scale, FA_DTYPE_FP16 if dtype == "f16" else FA_DTYPE_BF16,
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert _status(dbg) == 0, "a bounds check failed"
+    got = [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+    TB.check_gradients(a, do, got)
