@@ -952,7 +952,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step,
                 "note": ("fa_forward_host_packed: K requests in pinned host memory; libfa copies each in "
-                         "and out on its own streams through two device slots, overlapping the "
+                         "and out on its own streams through three device slots, overlapping the "
                          "neighbouring requests' kernels" if args.impl == "fused" and args.dtype != "e4m3"
                          else "torch copies around each call (pinned host buffers), nothing overlapped"),
                 "serial": e2e_serial},

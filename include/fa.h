@@ -134,11 +134,11 @@ int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* 
  * not copied back). dtype: FA_DTYPE_BF16 (fa_forward) or FA_DTYPE_FP16
  * (fa_forward_fp16). Host pointers need no alignment; page-locked memory
  * (cudaHostAlloc, cudaHostRegister) lets the copies run asynchronously.
- * Execution: each request's inputs are copied into one of two device slots
+ * Execution: each request's inputs are copied into one of three device slots
  * (stream-ordered memory from libfa's pool, on `stream`), the fused forward
  * runs on `stream`, and O, LSE are copied back. The copies run on two
- * library-owned streams of the current device, so request i+1's copy in and
- * request i-1's copy out overlap request i's kernels. Each tensor is its own
+ * library-owned streams of the current device, so later requests' copies in
+ * and earlier requests' copies out overlap request i's kernels. Each tensor is its own
  * copy (fa_forward_host_packed moves a request with one copy each way).
  * Ordering: all of it runs after the work already on `stream`, and work
  * enqueued on `stream` later runs after all of it; the call returns once

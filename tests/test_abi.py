@@ -151,6 +151,14 @@ def test_head_dim_256_only_on_the_forward(lib):
     assert plan == {"ctas": 2 * 4 * 3, "launches": 1, "workspace_bytes": 0}
 
 
+def _gpu_present():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
 def test_fp8_rejects(lib):
     def f(q=Q, k=K, v=V, o=O, l=L, Hq=2, Hkv=1, Nq=64, d=128, scale=0.1, ds=(1.0, 1.0, 1.0)):
         return lib.fa_forward_fp8(q, k, v, o, l, 1, Hq, Hkv, Nq, 64, d, 0, scale, *ds, None)
@@ -162,7 +170,8 @@ def test_fp8_rejects(lib):
     # o (BF16, 2 bytes per element) may not overlap q (1 byte per element): q spans
     # 2 * 64 * 128 bytes, so o may start right after it but not inside it
     assert f(o=Q + 64 * 128) == fa.FA_ERR_INVALID_ARG
-    assert f(o=Q + 2 * 64 * 128) != fa.FA_ERR_INVALID_ARG
+    if not _gpu_present():   # with a GPU, the made-up pointers then fail the device check
+        assert f(o=Q + 2 * 64 * 128) != fa.FA_ERR_INVALID_ARG
     assert f(q=0, k=0, v=0, o=0, l=0, Nq=0) == fa.FA_OK
 
 
