@@ -118,7 +118,9 @@ def test_split_merge_modes(fa, shape, cluster_merge, monkeypatch):
     B, Hq, Hkv, Nq, Nk, d, causal = shape
     a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=5, k_row_frac=0.01)
     plan = fa.fa_forward_plan(B, Hq, Hkv, Nq, Nk, d, causal)
-    blocks = B * Hq * ((Nq + 255) // 256)
+    # work units before splitting: 256-row query blocks, or KV heads on the decode
+    # path (at most 16 query rows read one KV head)
+    blocks = B * Hkv if (Hq // Hkv) * Nq <= 16 else B * Hq * ((Nq + 255) // 256)
     assert plan["ctas"] > blocks                     # the key ranges are split
     if cluster_merge:
         assert plan["launches"] == 1 and plan["workspace_bytes"] == 0
