@@ -583,16 +583,20 @@ int decode_cluster_capacity_t(int parts) {
 DecPlan decode_plan(long long heads, int n_chunks, int d, int sms, bool cluster_merge) {
   DecPlan pl{};
   // in-cluster merge: about 1.7 CTAs per SM in a single wave, i.e. parts per KV
-  // head = 1.7 SMs / heads rounded, between 1 and min(8, chunks) (8: a portable
-  // cluster). Measured on GB300 at batch 16 x 8 KV heads x 8192 keys (128 KV
-  // heads): 2 parts (256 CTAs) 6626 GB/s, 3: 6514, 5: 6255, 8 (two and a quarter
-  // waves of three CTAs per SM): 5956, 1 (fewer CTAs than SMs): 5776. A wave
-  // that stays resident to the end keeps HBM busiest; a partial last wave leaves
-  // it idle. One part needs no merge at all.
+  // head = 1.7 SMs / heads rounded, at least 1 and at most the head's chunks.
+  // Measured on GB300 at batch 16 x 8 KV heads x 8192 keys (128 KV heads): 2
+  // parts (256 CTAs) 6626 GB/s, 3: 6514, 5: 6255, 8 (two and a quarter waves of
+  // three CTAs per SM): 5956, 1 (fewer CTAs than SMs): 5776. A wave that stays
+  // resident to the end keeps HBM busiest; a partial last wave leaves it idle.
+  // More than 8 parts would exceed a portable cluster: with few KV heads and
+  // long keys the runs are merged by the merge kernel instead (below), unless a
+  // head has at most 8 chunks (one part each; the GPU cannot be filled anyway).
+  // One part needs no merge at all.
   if (cluster_merge) {
-    const int qmax = n_chunks < 8 ? n_chunks : 8;
     const long long want = (17ll * sms + 5 * heads) / (10 * heads);   // round(1.7 sms / heads)
-    const int parts = (int)(want < 1 ? 1 : (want > qmax ? qmax : want));
+    int parts = 0;
+    if (want <= 8) parts = (int)(want < 1 ? 1 : (want > n_chunks ? n_chunks : want));
+    else if (n_chunks <= 8) parts = n_chunks;
     if (parts > 0) {
       const int cpc = (n_chunks + parts - 1) / parts;
       const int np = (n_chunks + cpc - 1) / cpc;

@@ -85,7 +85,7 @@ SMALL = [
     (1, 2, 2, 16, 16, 64, True),        # square causal inside one chunk
     (1, 2, 1, 8, 5, 128, True),         # N_q > N_k: leading rows see no key
     (3, 8, 8, 1, 128, 128, False),      # exactly one chunk
-    # decode CTAs that walk runs of chunks (128 KV heads: runs of 2 chunks, ragged last run)
+    # decode CTAs that walk runs of chunks (128 KV heads: 2 runs of 17 and 16 chunks per head)
     (8, 32, 16, 4, 4100, 128, True),    # GQA 2 x 4 queries, causal
     (16, 8, 8, 1, 4200, 64, False),     # MQA-free, d = 64
 ]
@@ -213,6 +213,23 @@ def test_decode_b16_h32_kv8(fa):
     a = I.make_workload("decode_b16_h32_kv8_n8192_d128")
     o, lse = _run(fa, a)
     compare(o, lse, *run_oracle(a))
+
+
+DECODE_REGIMES = [
+    # (B, H_q, H_kv, N_q, N_k, d, causal), launches: how the decode plan splits each KV head
+    ((1, 8, 2, 1, 40000, 128, False), 2),   # 2 KV heads, 313 chunks: runs merged by the merge kernel
+    ((4, 32, 8, 1, 6000, 64, False), 1),    # 32 KV heads: 8 parts per head in clusters of 8
+    ((8, 16, 8, 2, 3000, 128, True), 1),    # 64 KV heads, 2 query rows each: 4 parts, causal
+    ((64, 32, 8, 1, 1000, 128, False), 1),  # 512 KV heads: one part each, no merge
+]
+
+
+@pytest.mark.parametrize("shape,launches", DECODE_REGIMES, ids=lambda s: "x".join(map(str, s[:6])) if isinstance(s, tuple) else None)
+def test_decode_plan_regimes(fa, shape, launches):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    assert fa.fa_forward_plan(B, Hq, Hkv, Nq, Nk, d, causal)["launches"] == launches
+    a = I.make_inputs(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=14, k_row_frac=0.01)
+    compare(*_run(fa, a), *run_oracle(a))
 
 
 def test_deterministic(fa):
