@@ -883,6 +883,33 @@ def main():
     flushed_ms = R.slowest_rank_ms(sum(e0.elapsed_time(e1) for e0, e1 in fev), world, dev)
     flushed_value = R.whole_job_rate(work_per_step, args.steps, flushed_ms, world)
 
+    # ---- the same steps captured once into a CUDA graph and replayed: no host
+    # enqueue per call, which is what bounds the smallest workloads
+    graph = None
+    if args.impl == "fused":
+        n_cap = min(args.steps, 100)
+        reps = max(1, args.steps // n_cap)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_cap):
+                step(i)
+        g.replay()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch)
+        g0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        barrier()
+        if fa.fa_device_status() != fa.FA_OK:
+            raise RuntimeError("a kernel reported a timed-out wait during the graph replays")
+        g_ms = R.slowest_rank_ms(g0.elapsed_time(g1), world, dev)
+        graph = {"value": R.whole_job_rate(work_per_step, n_cap * reps, g_ms, world), "unit": unit,
+                 "ms_per_step": g_ms / (n_cap * reps),
+                 "note": f"the same steps captured once into a CUDA graph of {n_cap} calls, replayed {reps} times"}
+        del g
+
     # ---- end to end through the C ABI with host buffers: every step copies its
     # inputs in from pinned host memory and its O | LSE back out, inside the
     # timed region (fa_forward_host_packed; see time_e2e)
@@ -957,6 +984,7 @@ def main():
                          else "torch copies around each call (pinned host buffers), nothing overlapped"),
                 "serial": e2e_serial},
         "gpu_launches": kernels_per_step * args.steps,
+        "graph": graph,
         "flushed": {"value": flushed_value, "unit": unit, "ms_per_step": flushed_ms / args.steps,
                     "note": ("each step alone between its own events, L2 flushed (256 MiB write) "
                              "before it, outside the events")},
