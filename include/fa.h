@@ -82,8 +82,12 @@ typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 } fa_dtype;
  * previous kernel on the stream, and it reads and writes global memory only
  * after that kernel has completed.
  * Decode / few queries (the H_q/H_kv * N_q query rows that share a KV head
- * number at most 16): one CTA per (batch, KV head, 128-key chunk) reads its
- * K and V chunk once for all those rows; chunk partials are merged the same way.
+ * number at most 16): one CTA per (batch, KV head, run of consecutive 128-key
+ * chunks) reads each K and V chunk once for all those rows, the runs sized so
+ * that the grid is about 1.7 CTAs per SM; run partials are merged the same way
+ * (in a cluster when a KV head has at most 8 runs, else by a second kernel).
+ * Every call can be captured into a CUDA graph once a first call has run on
+ * the device outside the capture (it does one-time set-up).
  * Head dimension 256: one CTA per 128-row query tile (a 256-column output tile
  * fills half of the SM's tensor memory), two 128-key score buffers in turn,
  * K and V in 128-column halves; no key-range split, no workspace, one launch.
