@@ -780,16 +780,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j > 0) rescale_o<D>(tO, alpha);   // O_X holds PV_X(0..j-1), stable (S_X(j) commit)
         }
-        const float mb = m_ref == -INFINITY ? 0.f : m_ref;
-        const float r1 = exp_half<E>(s, c, mb, tS);
-        publish(bar(C::kBarP1 + X));
-        const float r2 = exp_half<E>(s + 64, c, mb, tS + C::kPHalfCols);
-        publish(bar(C::kBarP2 + X));
-        l += r1 + r2;
-      } else {
-        // the first half's P against the reference, and the second half's max:
-        // any rescale is decided here, while O_X is stable (S_X(j) commit)
-        float r1 = exp_half<E>(s, c, m_ref, tS);
+      }
+      // The first half's P against the reference (0 for a row that has none).
+      // Both paths share this code and the second half's below: one copy of each
+      // in the kernel keeps its main loop small.
+      float r1 = exp_half<E>(s, c, m_ref == -INFINITY ? 0.f : m_ref, tS);
+      if (spec) {
+        // and the second half's max: any rescale is decided here, while O_X is
+        // stable (S_X(j) commit)
         const float m2 = max_scores<kTileN / 2>(s + 64) * c;
         const bool need = !(r1 <= Lag<E>::kSumCap) || m2 > m_ref + Lag<E>::kTau;
         if (__any_sync(0xffffffffu, need)) {
@@ -803,12 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale_o<D>(tO, alpha);
           r1 = exp_half<E>(s, c, m_ref, tS);
         }
-        publish(bar(C::kBarP1 + X));
-        // the second half's P <= 2^kTau now
-        const float r2 = exp_half<E>(s + 64, c, m_ref, tS + C::kPHalfCols);
-        publish(bar(C::kBarP2 + X));
-        l += r1 + r2;
       }
+      publish(bar(C::kBarP1 + X));
+      // the second half's P <= 2^kTau now
+      const float r2 = exp_half<E>(s + 64, c, m_ref == -INFINITY ? 0.f : m_ref, tS + C::kPHalfCols);
+      publish(bar(C::kBarP2 + X));
+      l += r1 + r2;
     }
     if (ok && n_loop > 0) {
       ok = mbar_wait(bar(C::kBarO), 0, s_abort, p.status);
