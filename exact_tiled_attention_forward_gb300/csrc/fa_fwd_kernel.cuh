@@ -784,23 +784,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The first half's P against the reference (0 for a row that has none).
       // Both paths share this code and the second half's below: one copy of each
       // in the kernel keeps its main loop small.
-      float r1 = exp_half<E>(s, c, m_ref == -INFINITY ? 0.f : m_ref, tS);
-      if (spec) {
-        // and the second half's max: any rescale is decided here, while O_X is
-        // stable (S_X(j) commit)
+      // On the later tiles the second half's max then decides any rescale, while
+      // O_X is stable (S_X(j) commit); a rescale redoes the first half (the same
+      // copy of the code, a second pass).
+      float r1;
+#pragma unroll 1
+      for (int pass = 0;; ++pass) {
+        r1 = exp_half<E>(s, c, m_ref == -INFINITY ? 0.f : m_ref, tS);
+        if (!spec || pass > 0) break;
         const float m2 = max_scores<kTileN / 2>(s + 64) * c;
         const bool need = !(r1 <= Lag<E>::kSumCap) || m2 > m_ref + Lag<E>::kTau;
-        if (__any_sync(0xffffffffu, need)) {
-          float alpha = 1.f;
-          if (need) {
-            const float m_new = fmaxf(m_ref, fmaxf(max_scores<kTileN / 2>(s) * c, m2));
-            alpha = ex2_approx(m_ref - m_new);
-            m_ref = m_new;
-            l *= alpha;
-          }
-          rescale_o<D>(tO, alpha);
-          r1 = exp_half<E>(s, c, m_ref, tS);
+        if (!__any_sync(0xffffffffu, need)) break;
+        float alpha = 1.f;
+        if (need) {
+          const float m_new = fmaxf(m_ref, fmaxf(max_scores<kTileN / 2>(s) * c, m2));
+          alpha = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
         }
+        rescale_o<D>(tO, alpha);
       }
       publish(bar(C::kBarP1 + X));
       // the second half's P <= 2^kTau now
