@@ -144,6 +144,13 @@ struct Cfg {
 };
 
 __device__ __forceinline__ int min_i(int a, int b) { return a < b ? a : b; }
+// How a tile step treats the mask: never, always, or as the tile needs
+// (checked at run time).
+enum class MaskMode { kNone, kAlways, kCheck };
+template <MaskMode M>
+struct MaskTag {
+  static constexpr MaskMode value = M;
+};
 __device__ __forceinline__ int max_i(int a, int b) { return a > b ? a : b; }
 
 // P = 2^(s*c - mb) for 64 scores of this thread's row (FP32 pairs, one packed
@@ -742,14 +749,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = mbar_wait(bar(C::kBarS + X), (uint32_t)j & 1u, s_abort, p.status))) break;
+    // One tile of the key range (j).
+    auto tile_step = [&](int j, auto mask_tag) -> bool {
+      constexpr MaskMode kMask = decltype(mask_tag)::value;
+      if (!(ok = mbar_wait(bar(C::kBarS + X), (uint32_t)j & 1u, s_abort, p.status))) return false;
       tc_fence_after();
       float s[kTileN];
       if (!FA_DBG_OK(p.status, tmem_in(lane_base + C::tm_s(X), kTileN) &&
                                    tmem_in(lane_base + C::tm_o(X), D))) {
         ok = false;   // FA_DEBUG: reported; this tile is not processed
-        break;
+        return false;
       }
       tmem_ld32(tS + 0, s);
       tmem_ld32(tS + 32, s + 32);
@@ -758,7 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       const int key0 = (lo + j) * kTileN;
       // mask: ragged key tail, and keys after the causal diagonal
-      if (key0 + kTileN > p.N_k || (p.causal && key0 + kTileN - 1 > tile_first_row + p.kv_off)) {
+      if (kMask == MaskMode::kAlways ||
+          (kMask == MaskMode::kCheck &&
+           (key0 + kTileN > p.N_k || (p.causal && key0 + kTileN - 1 > tile_first_row + p.kv_off)))) {
         int lim = p.N_k - key0;
         if (p.causal) lim = min_i(lim, row + p.kv_off + 1 - key0);
 #pragma unroll
@@ -809,6 +820,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float r2 = exp_half<E>(s + 64, c, m_ref == -INFINITY ? 0.f : m_ref, tS + C::kPHalfCols);
       publish(bar(C::kBarP2 + X));
       l += r1 + r2;
+      return true;
+    };
+    auto masked_at = [&](int j) {
+      const int key0 = (lo + j) * kTileN;
+      return key0 + kTileN > p.N_k || (p.causal && key0 + kTileN - 1 > tile_first_row + p.kv_off);
+    };
+    if constexpr (E == Elem::E4M3) {
+      // FP8 (bound by this loop): tiles that need a mask only come at the end of
+      // a range, so they run in a second loop with its own copy of the step and
+      // the main loop's copy has no mask code (1558 -> 1699 TFLOP/s at 32 heads x
+      // 4096; the same split made the BF16 kernel 1-2.5 % slower)
+      int j = 0;
+      for (; j < n && !masked_at(j); ++j)
+        if (!tile_step(j, MaskTag<MaskMode::kNone>{})) break;
+      if (ok)
+        for (; j < n; ++j)
+          if (!tile_step(j, MaskTag<MaskMode::kAlways>{})) break;
+    } else {
+      for (int j = 0; j < n; ++j)
+        if (!tile_step(j, MaskTag<MaskMode::kCheck>{})) break;
     }
     if (ok && n_loop > 0) {
       ok = mbar_wait(bar(C::kBarO), 0, s_abort, p.status);
